@@ -1,0 +1,172 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn: grouped-query attention over a block-paged
+ * KV cache, hand-written CUDA for GB300 (sm_103a).
+ *
+ * The operation.  The pages "Qwen3-4B / 8B / 32B" (section "Architecture Notes")
+ * describe full attention with grouped-query attention -- Qwen3-4B: 32 query heads
+ * over 8 KV heads, head dim 128; Qwen3-32B: 64 query heads, group 8 -- served from a
+ * paged KV cache with prefix caching; section "Qwen3-32B Serving Load" gives a KV
+ * budget of 21.4 GB = 5360 blocks for Qwen3-32B, which fixes 16-token blocks; section
+ * "Warm Prefix-Cache TTFT" is the chunked prefill over a warm prefix.  For query head
+ * h of a sequence, with g = num_heads / num_kv_heads and kv head h / g:
+ *
+ *     o = sum_{t in keys} softmax_t(scale * <q, K_t>) V_t
+ *
+ * K_t, V_t read at pool[block_tables[s][t / 16], h / g, t % 16, :].  Softmax in fp32
+ * (online, base 2), bf16 inputs, bf16 output rounded to nearest even.
+ *
+ * Memory.  Every pointer argument is a DEVICE pointer of the current CUDA device
+ * unless stated otherwise; the caller allocates and owns every buffer (the library
+ * allocates no device memory).  Every call is asynchronous on `stream` (NULL = the
+ * legacy default stream) and returns after the launch: the return code reports host
+ * validation and launch errors only.  Problems the device finds (a block id or slot
+ * outside the pool, a pipeline wait that timed out) set bits of a device status word
+ * that pa_device_status() reads.  Calls are thread-safe.
+ *
+ * Layouts (all row-major, contiguous):
+ *   pool K, V      [num_blocks, num_kv_heads, 16, head_dim]   bf16, 16-byte aligned
+ *   slot           block_id * 16 + offset_in_block
+ *   block_tables   [batch, max_blocks] int32; entries past ceil(seq_len / 16) are never read
+ *   seq_lens       [batch] int32, tokens in the sequence including any appended this step
+ *   q, out         decode [batch, num_heads, head_dim]; prefill [sum of chunk lengths,
+ *                  num_heads, head_dim]; bf16, 16-byte aligned
+ *
+ * Supported: block_size 16; head_dim 64 or 128; any group size for prefill, group
+ * size <= 16 for decode; batch <= 65535.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t. */
+typedef struct CUstream_st *pa_stream_t;
+
+enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,  /* host validation failed; nothing was launched */
+    PA_ERR_UNSUPPORTED = -2,  /* block size, head dim or group size outside the compiled set */
+    PA_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
+    PA_ERR_OUT_OF_RANGE = -4, /* pa_device_status: a block id / slot / length outside the pool was skipped */
+    PA_ERR_TIMEOUT = -5       /* pa_device_status: a pipeline wait ran out (a bug, never expected) */
+};
+
+/* Device status bits reported by pa_device_status. */
+#define PA_DEV_OUT_OF_RANGE 1u
+#define PA_DEV_TIMEOUT 2u
+
+/* The paged KV pool: two device tensors [num_blocks, num_kv_heads, block_size, head_dim] bf16. */
+typedef struct {
+    void *k_cache;
+    void *v_cache;
+    int32_t num_blocks;
+    int32_t block_size;   /* must be 16 */
+    int32_t num_kv_heads;
+    int32_t head_dim;     /* 64 or 128 */
+} pa_pool;
+
+/*
+ * pa_kv_append -- write new K/V rows into their pool slots.
+ * Defines: for t in [0, num_tokens) with slot_mapping[t] >= 0,
+ *   k_cache[slot / 16, h, slot % 16, :] = k_new[t, h, :]  (and v likewise), every kv head h.
+ * This is how a decode token or a prefill chunk enters the paged cache ("Qwen3-4B / 8B /
+ * 32B", "Architecture Notes": paged KV cache; "Warm Prefix-Cache TTFT": only new tokens
+ * are written on a prefix hit).  It must precede, on the same stream, the attention call
+ * that reads those tokens.
+ *   k_new, v_new   [num_tokens, num_kv_heads, head_dim] bf16, 16-byte aligned
+ *   slot_mapping   [num_tokens] int64; < 0 skips the row; >= num_blocks*16 is skipped and
+ *                  sets PA_DEV_OUT_OF_RANGE.  Duplicate slots are a caller error.
+ * Bit-exact copy.  num_tokens == 0 is a no-op.
+ */
+int pa_kv_append(const pa_pool *pool, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                 int32_t num_tokens, pa_stream_t stream);
+
+/*
+ * pa_decode -- one query token per sequence attends to keys [0, seq_lens[b]).
+ * ("Qwen3-4B / 8B / 32B", "Architecture Notes": GQA over a paged KV cache; the query is
+ * the newest token, already appended.)
+ *   q, out         [batch, num_heads, head_dim] bf16
+ *   scale          softmax scale, normally 1/sqrt(head_dim)
+ * seq_lens[b] == 0 gives a zero row.  seq_lens[b] outside [0, max_blocks*16] is clamped
+ * and sets PA_DEV_OUT_OF_RANGE.  When batch * num_kv_heads is small the library splits
+ * each sequence over a thread-block cluster and merges in on-chip memory (no workspace).
+ */
+int pa_decode(const pa_pool *pool, const void *q, const int32_t *block_tables, int32_t max_blocks,
+              const int32_t *seq_lens, int32_t batch, int32_t num_heads, float scale, void *out,
+              pa_stream_t stream);
+
+/*
+ * Workspace of pa_decode_splitkv, in bytes: ws_o [batch, num_heads, P, head_dim] fp32
+ * followed by ws_lse [batch, num_heads, P] fp32 (ws_lse may live anywhere 16-byte aligned;
+ * this is their sum).  Host-only, no CUDA call.
+ */
+size_t pa_splitkv_workspace_bytes(int32_t batch, int32_t num_heads, int32_t head_dim, int32_t num_partitions);
+
+/*
+ * pa_decode_splitkv -- flash-decoding partitions of the decode above.  Partition p of P
+ * covers logical blocks [p*ceil(nb/P), (p+1)*ceil(nb/P)) of the nb = ceil(seq_len/16)
+ * blocks and writes its own normalised output O_p and natural-log log-sum-exp
+ * lse_p = m_p + ln(l_p) of its scaled scores; an empty partition writes O_p = 0,
+ * lse_p = -inf.  (Long-context decode: the pages' long prompts are 4097-16384 tokens,
+ * "Warm Prefix-Cache TTFT" and the 4097/8192-token golden prompts.)
+ *   num_partitions P in [1, 4096]
+ *   ws_o           [batch, num_heads, P, head_dim] fp32, 16-byte aligned (scratch owned by caller)
+ *   ws_lse         [batch, num_heads, P] fp32
+ */
+int pa_decode_splitkv(const pa_pool *pool, const void *q, const int32_t *block_tables, int32_t max_blocks,
+                      const int32_t *seq_lens, int32_t batch, int32_t num_heads, float scale,
+                      int32_t num_partitions, float *ws_o, float *ws_lse, pa_stream_t stream);
+
+/*
+ * pa_combine -- log-sum-exp merge of split-KV partitions:
+ *   M = max_p lse_p;  w_p = exp(lse_p - M);  out = sum_p w_p O_p / sum_p w_p
+ * (partitions with lse_p = -inf weigh 0; all empty gives a zero row).
+ *   ws_o, ws_lse   as written by pa_decode_splitkv;  out [batch, num_heads, head_dim] bf16
+ */
+int pa_combine(const float *ws_o, const float *ws_lse, int32_t batch, int32_t num_heads, int32_t head_dim,
+               int32_t num_partitions, void *out, pa_stream_t stream);
+
+/*
+ * pa_prefill_chunked -- a causal query chunk over a cached paged prefix plus itself.
+ * Sequence b's chunk is q rows [cu_q_lens[b], cu_q_lens[b+1]) (C_b tokens); seq_lens[b]
+ * counts the prefix AND the chunk (whose K/V pa_kv_append already wrote).  Chunk query i
+ * sits at position seq_lens[b] - C_b + i and attends to keys 0 .. that position.
+ * ("Qwen3-4B / 8B / 32B", "Warm Prefix-Cache TTFT": warm prefix hit, only the new chunk
+ * is computed.)
+ *   q, out         [cu_q_lens[batch], num_heads, head_dim] bf16
+ *   cu_q_lens      [batch + 1] int32, non-decreasing, cu_q_lens[0] = 0
+ *   max_chunk      an upper bound of max_b C_b (sizes the grid; rows beyond C_b are idle)
+ * A sequence with C_b > seq_lens[b] or seq_lens[b] > max_blocks*16 is skipped and sets
+ * PA_DEV_OUT_OF_RANGE.
+ */
+int pa_prefill_chunked(const pa_pool *pool, const void *q, const int32_t *cu_q_lens, const int32_t *block_tables,
+                       int32_t max_blocks, const int32_t *seq_lens, int32_t batch, int32_t num_heads,
+                       int32_t max_chunk, float scale, void *out, pa_stream_t stream);
+
+/*
+ * pa_device_status -- synchronise `stream`, then read the device status word of the
+ * current device into *flags (PA_DEV_* bits, 0 = clean), clearing it when `clear` != 0.
+ * Returns PA_OK, PA_ERR_OUT_OF_RANGE or PA_ERR_TIMEOUT according to the bits (timeout
+ * first), PA_ERR_INVALID_ARG for a NULL flags pointer, PA_ERR_CUDA on a CUDA error.
+ */
+int pa_device_status(uint32_t *flags, int32_t clear, pa_stream_t stream);
+
+/* Number of cluster splits pa_decode uses for this shape on the current device. */
+int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
+
+/* Human-readable name of a status code (static string). */
+const char *pa_status_str(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,220 @@
+"""Python binding of libpagedattn (paged GQA attention for GB300).
+
+Argument marshalling only: torch tensors become device pointers and sizes for the
+C ABI in include/pagedattn.h; every step of the computation runs in the CUDA
+kernels of libpagedattn.so.  There is no CPU or PyTorch fallback -- if the
+library is not built, loading it raises.
+
+Names follow the C ABI: pa_kv_append, pa_decode, pa_decode_splitkv,
+pa_combine, pa_prefill_chunked, pa_device_status.  Tensors must be CUDA,
+contiguous, and of the dtypes the header states (bf16 data, int32 tables,
+int64 slot mapping, fp32 split-KV workspace).  Calls are asynchronous on the
+given stream (default: torch's current stream).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_decode_splitkv", "pa_combine", "pa_prefill_chunked",
+           "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "PagedAttnError",
+           "library", "library_path", "BLOCK_SIZE", "EXPORTED_SYMBOLS"]
+
+BLOCK_SIZE = 16
+PKG = Path(__file__).resolve().parent
+_LIB_PATH = PKG / "libpagedattn.so"
+EXPORTED_SYMBOLS = ("pa_kv_append", "pa_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv", "pa_combine",
+                    "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_status_str",
+                    "pa_version")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = -1
+PA_ERR_UNSUPPORTED = -2
+PA_ERR_CUDA = -3
+PA_ERR_OUT_OF_RANGE = -4
+PA_ERR_TIMEOUT = -5
+PA_DEV_OUT_OF_RANGE = 1
+PA_DEV_TIMEOUT = 2
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, what: str, code: int):
+        super().__init__(f"{what} failed: {_status_str(code)} ({code})")
+        self.code = code
+
+
+class _PaPoolC(ctypes.Structure):
+    _fields_ = [("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("num_blocks", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library_path() -> Path:
+    return _LIB_PATH
+
+
+def library() -> ctypes.CDLL:
+    """Load libpagedattn.so (built by paged_kv_gqa_slot_gb300.build); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not _LIB_PATH.exists():
+        raise RuntimeError(f"{_LIB_PATH} is not built; run `python -m paged_kv_gqa_slot_gb300.build` "
+                           "(or __graft_entry__.build()) first -- there is no fallback path")
+    lib = ctypes.CDLL(str(_LIB_PATH))
+    P, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+    pool = ctypes.POINTER(_PaPoolC)
+    sig = {
+        "pa_kv_append": (ctypes.c_int, [pool, P, P, P, I32, P]),
+        "pa_decode": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, P, P]),
+        "pa_splitkv_workspace_bytes": (SZ, [I32, I32, I32, I32]),
+        "pa_decode_splitkv": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, I32, P, P, P]),
+        "pa_combine": (ctypes.c_int, [P, P, I32, I32, I32, I32, P, P]),
+        "pa_prefill_chunked": (ctypes.c_int, [pool, P, P, P, I32, P, I32, I32, I32, F32, P, P]),
+        "pa_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32, P]),
+        "pa_decode_num_splits": (ctypes.c_int, [I32, I32, I32]),
+        "pa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+        "pa_version": (ctypes.c_int, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _status_str(code: int) -> str:
+    try:
+        return library().pa_status_str(code).decode()
+    except Exception:  # pragma: no cover - used while raising
+        return str(code)
+
+
+def _check(code: int, what: str) -> None:
+    if code != PA_OK:
+        raise PagedAttnError(what, code)
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str) -> int:
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: need a contiguous CUDA {dtype} tensor, got {t.dtype} on {t.device}")
+    return t.data_ptr()
+
+
+class PaPool:
+    """The paged KV pool: k_cache, v_cache = [num_blocks, num_kv_heads, 16, head_dim] bf16 on the GPU."""
+
+    def __init__(self, k_cache: torch.Tensor, v_cache: torch.Tensor):
+        if k_cache.shape != v_cache.shape or k_cache.dim() != 4:
+            raise ValueError("k_cache and v_cache must both be [num_blocks, num_kv_heads, block_size, head_dim]")
+        self.k_cache, self.v_cache = k_cache, v_cache
+        nb, hkv, bs, d = k_cache.shape
+        self.c = _PaPoolC(_dev(k_cache, torch.bfloat16, "k_cache"), _dev(v_cache, torch.bfloat16, "v_cache"),
+                          nb, bs, hkv, d)
+        self.ref = ctypes.byref(self.c)
+
+    @property
+    def num_kv_heads(self) -> int:
+        return self.c.num_kv_heads
+
+    @property
+    def head_dim(self) -> int:
+        return self.c.head_dim
+
+
+def pa_kv_append(pool: PaPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                 stream=None) -> None:
+    T = int(slot_mapping.numel())
+    rc = library().pa_kv_append(pool.ref, _dev(k_new, torch.bfloat16, "k_new") if T else None,
+                                _dev(v_new, torch.bfloat16, "v_new") if T else None,
+                                _dev(slot_mapping, torch.int64, "slot_mapping") if T else None, T, _stream(stream))
+    _check(rc, "pa_kv_append")
+
+
+def pa_decode(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    B, Hq, _ = q.shape
+    out = torch.empty_like(q) if out is None else out
+    rc = library().pa_decode(pool.ref, _dev(q, torch.bfloat16, "q"), _dev(block_tables, torch.int32, "block_tables"),
+                             block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale),
+                             _dev(out, torch.bfloat16, "out"), _stream(stream))
+    _check(rc, "pa_decode")
+    return out
+
+
+def pa_splitkv_workspace_bytes(batch: int, num_heads: int, head_dim: int, num_partitions: int) -> int:
+    return int(library().pa_splitkv_workspace_bytes(batch, num_heads, head_dim, num_partitions))
+
+
+def pa_decode_splitkv(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                      scale: float, num_partitions: int, ws_o: Optional[torch.Tensor] = None,
+                      ws_lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    B, Hq, D = q.shape
+    P = int(num_partitions)
+    if ws_o is None:
+        ws_o = torch.empty((B, Hq, P, D), dtype=torch.float32, device=q.device)
+    if ws_lse is None:
+        ws_lse = torch.empty((B, Hq, P), dtype=torch.float32, device=q.device)
+    rc = library().pa_decode_splitkv(pool.ref, _dev(q, torch.bfloat16, "q"),
+                                     _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                     _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale), P,
+                                     _dev(ws_o, torch.float32, "ws_o"), _dev(ws_lse, torch.float32, "ws_lse"),
+                                     _stream(stream))
+    _check(rc, "pa_decode_splitkv")
+    return ws_o, ws_lse
+
+
+def pa_combine(ws_o: torch.Tensor, ws_lse: torch.Tensor, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    B, Hq, P, D = ws_o.shape
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=ws_o.device) if out is None else out
+    rc = library().pa_combine(_dev(ws_o, torch.float32, "ws_o"), _dev(ws_lse, torch.float32, "ws_lse"), B, Hq, D, P,
+                              _dev(out, torch.bfloat16, "out"), _stream(stream))
+    _check(rc, "pa_combine")
+    return out
+
+
+def pa_prefill_chunked(pool: PaPool, q: torch.Tensor, cu_q_lens: torch.Tensor, block_tables: torch.Tensor,
+                       seq_lens: torch.Tensor, scale: float, max_chunk: int, out: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    _, Hq, _ = q.shape
+    B = int(seq_lens.numel())
+    out = torch.empty_like(q) if out is None else out
+    rc = library().pa_prefill_chunked(pool.ref, _dev(q, torch.bfloat16, "q"), _dev(cu_q_lens, torch.int32, "cu_q_lens"),
+                                      _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                      _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, int(max_chunk), float(scale),
+                                      _dev(out, torch.bfloat16, "out"), _stream(stream))
+    _check(rc, "pa_prefill_chunked")
+    return out
+
+
+def pa_device_status(clear: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the device status bits (0 = clean)."""
+    flags = ctypes.c_uint32(0)
+    rc = library().pa_device_status(ctypes.byref(flags), 1 if clear else 0, _stream(stream))
+    if rc == PA_ERR_CUDA:
+        raise PagedAttnError("pa_device_status", rc)
+    return int(flags.value)
+
+
+def pa_decode_num_splits(batch: int, num_kv_heads: int, max_blocks: int) -> int:
+    return int(library().pa_decode_num_splits(batch, num_kv_heads, max_blocks))
+
+
+def default_scale(head_dim: int) -> float:
+    return 1.0 / math.sqrt(head_dim)

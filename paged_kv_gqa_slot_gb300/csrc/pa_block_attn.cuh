@@ -1,0 +1,267 @@
+// pa_block_attn.cuh -- the paged-KV pipeline shared by the decode, split-KV and
+// warp-MMA prefill kernels.
+//
+// Producer: one warp walks a sequence's block table (32 entries per coalesced load,
+// the next 32 prefetched) and, for each logical block, has one lane issue TMA loads of
+// the (block, kv head) K tile and V tile into a ring slot of shared memory.  Each tile
+// is [16 tokens x D] bf16 = one contiguous 2 or 4 KB run of the pool, loaded as D/64
+// boxes of 16 rows x 128 B with 128-byte swizzling.  The block id is only a row
+// coordinate of the tensor map, so paging costs nothing beyond the table read.
+//
+// Consumer: a warp owns a 16-row tile of (query, head) rows.  Per 16-token block it
+// computes S = Q K^T with mma.m16n8k16 (Q fragments stay in registers), masks, updates
+// the running max / sum (online softmax in base 2, fp32), rounds P to bf16 and
+// accumulates O += P V with the same MMA, reading K and V with ldmatrix (V transposed).
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+template <int D>
+struct KvTile {
+    static constexpr int kHalves = D / 64;                 // 64-column (128-byte) TMA boxes per tile
+    static constexpr int kBoxBytes = kBlockSize * 128;     // 2048
+    static constexpr int kTileBytes = kBlockSize * D * 2;  // one (block, kv head) tile of K or of V
+    static constexpr int kStageBytes = 2 * kTileBytes;     // K tile then V tile
+};
+
+// Issue the TMA loads of logical blocks [blk0, blk0 + n) of one sequence into a ring of
+// kStages slots.  Called by a whole warp; returns false if a wait timed out.  On return
+// every copy it issued has landed (or the wait for it timed out), so the caller may exit.
+template <int D, int kStages>
+__device__ __forceinline__ bool produce_kv_blocks(uint8_t* ring, uint64_t* full, uint64_t* empty,
+                                                  const CUtensorMap* tm_k, const CUtensorMap* tm_v,
+                                                  const int32_t* bt, int n, int num_blocks, int num_kv_heads,
+                                                  int kvh, unsigned* status, uint64_t policy) {
+    using T = KvTile<D>;
+    const int lane = threadIdx.x & 31;
+    int next = (lane < n) ? __ldg(bt + lane) : 0;
+    bool ok = true;
+    int issued = 0;
+    for (int c0 = 0; c0 < n && ok; c0 += 32) {
+        int cur = next;
+        if (c0 + 32 + lane < n) next = __ldg(bt + c0 + 32 + lane);
+        if (c0 + lane < n && (cur < 0 || cur >= num_blocks)) {
+            atomicOr(status, kDevOutOfRange);
+            cur = 0;  // keep the copy inside the pool; the status word reports the bad id
+        }
+        const int cnt = min(32, n - c0);
+        for (int j = 0; j < cnt; ++j) {
+            const int blk = __shfl_sync(0xffffffffu, cur, j);
+            const int i = c0 + j;
+            const int st = i % kStages;
+            if (lane == 0) {
+                if (i >= kStages) ok = mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1);
+                if (ok) {
+                    mbar_arrive_expect_tx(&full[st], T::kStageBytes);
+                    const int row = (blk * num_kv_heads + kvh) * kBlockSize;
+                    uint8_t* kd = ring + st * T::kStageBytes;
+                    uint8_t* vd = kd + T::kTileBytes;
+#pragma unroll
+                    for (int h = 0; h < T::kHalves; ++h) {
+                        tma_load_2d(kd + h * T::kBoxBytes, tm_k, h * 64, row, &full[st], policy);
+                        tma_load_2d(vd + h * T::kBoxBytes, tm_v, h * 64, row, &full[st], policy);
+                    }
+                    ++issued;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+            if (!ok) break;
+        }
+    }
+    // every copy this warp issued must have landed before the CTA may leave
+    if (lane == 0) {
+        for (int i = max(0, issued - kStages); i < issued; ++i)
+            if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) ok = false;
+        if (!ok) atomicOr(status, kDevTimeout);
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Running softmax state of the two rows a thread touches (row lane/4 and lane/4 + 8).
+struct RowState {
+    float m_a, l_a, m_b, l_b;
+    __device__ __forceinline__ void init() {
+        m_a = -INFINITY;
+        l_a = 0.f;
+        m_b = -INFINITY;
+        l_b = 0.f;
+    }
+};
+
+// Fragments of a warp's 16-row tile.  With TWO_ROWS the tile uses all 16 MMA rows
+// (lane/4 and lane/4 + 8); without it only rows 0..7 carry data (a group of <= 8 query
+// heads) and the A/C registers of rows 8..15 are never materialised: the MMA reads zero
+// for them and its row 8..15 outputs are dead values.
+template <bool TWO_ROWS>
+struct Rows {
+    static constexpr int kA = TWO_ROWS ? 4 : 2;  // A registers per 16-wide k step
+    static constexpr int kC = TWO_ROWS ? 4 : 2;  // C registers per 8-wide n tile
+};
+
+// c[16x8] += a[16x16] * b[16x8] (bf16 in, fp32 accumulate) on the tile's live rows.
+template <bool TWO_ROWS>
+__device__ __forceinline__ void mma_rows(float (&c)[Rows<TWO_ROWS>::kC], const uint32_t (&a)[Rows<TWO_ROWS>::kA],
+                                         uint32_t b0, uint32_t b1) {
+    if constexpr (TWO_ROWS) {
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        float d2, d3;
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %6, %5, %6}, {%7, %8}, "
+            "{%0, %1, %9, %9};"
+            : "+f"(c[0]), "+f"(c[1]), "=f"(d2), "=f"(d3)
+            : "r"(a[0]), "r"(a[1]), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+    }
+}
+
+// Online-softmax update of one row from its four scores in this thread (keys t0, t0+1,
+// t0+8, t0+9 of the block); returns the two packed bf16 P pairs and rescales o_row.
+struct RowUpdate {
+    uint32_t p01, p89;
+    float alpha;
+};
+__device__ __forceinline__ RowUpdate row_update(float& m, float& l, float s0, float s1, float s8, float s9, int t0,
+                                                int lim, float scale_log2) {
+    float x0 = t0 < lim ? s0 * scale_log2 : -INFINITY;
+    float x1 = t0 + 1 < lim ? s1 * scale_log2 : -INFINITY;
+    float x2 = t0 + 8 < lim ? s8 * scale_log2 : -INFINITY;
+    float x3 = t0 + 9 < lim ? s9 * scale_log2 : -INFINITY;
+    float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(m, mx);
+    const float base = mn == -INFINITY ? 0.f : mn;  // a row that has seen no key yet
+    RowUpdate u;
+    u.alpha = fast_exp2(m - base);
+    x0 = fast_exp2(x0 - base);
+    x1 = fast_exp2(x1 - base);
+    x2 = fast_exp2(x2 - base);
+    x3 = fast_exp2(x3 - base);
+    l = l * u.alpha + ((x0 + x1) + (x2 + x3));
+    m = mn;
+    u.p01 = pack_bf16x2(x0, x1);
+    u.p89 = pack_bf16x2(x2, x3);
+    return u;
+}
+
+// One 16-token block for one warp's 16-row tile.
+//   ks, vs   : shared addresses of the K and V tiles of the ring slot
+//   qa       : Q A-fragments of the warp's rows, [D/16][kA]
+//   o        : O accumulators, [D/8][kC] (C-fragment layout)
+//   lim_a/b  : keys with in-block index < lim are visible to row a (lane/4) / row b
+//              (lane/4 + 8); <= 0 means none
+//   vlim     : rows >= vlim of the slot lie past the sequence end; whatever they hold
+//              (stale data, even NaN) is zeroed in the V fragments, since P = 0 times
+//              NaN would still poison O.  K needs no such care: masked scores are
+//              replaced, not scaled.
+template <int D, bool TWO_ROWS>
+__device__ __forceinline__ void block_step(uint32_t ks, uint32_t vs,
+                                           const uint32_t (&qa)[D / 16][Rows<TWO_ROWS>::kA],
+                                           float (&o)[D / 8][Rows<TWO_ROWS>::kC], RowState& rs, int lim_a,
+                                           int lim_b, int vlim, float scale_log2) {
+    constexpr int kC = Rows<TWO_ROWS>::kC;
+    const int lane = threadIdx.x & 31;
+    float s0[kC], s1[kC];
+#pragma unroll
+    for (int j = 0; j < kC; ++j) s0[j] = s1[j] = 0.f;
+    {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int tok = rr + ((mi >> 1) << 3);  // matrices 0,1: tokens 0-7; 2,3: tokens 8-15
+        const int csel = mi & 1;                // matrices 0,2: first 8 columns of the k-step
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const int chunk = kk * 2 + csel;
+            const uint32_t addr = ks + (chunk >> 3) * KvTile<D>::kBoxBytes + swz128(tok, chunk & 7);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(addr, b0, b1, b2, b3);
+            mma_rows<TWO_ROWS>(s0, qa[kk], b0, b1);
+            mma_rows<TWO_ROWS>(s1, qa[kk], b2, b3);
+        }
+    }
+    const int t0 = (lane & 3) * 2;  // this thread's key columns: t0, t0+1, t0+8, t0+9
+    uint32_t pa[Rows<TWO_ROWS>::kA];
+    {
+        const RowUpdate u = row_update(rs.m_a, rs.l_a, s0[0], s0[1], s1[0], s1[1], t0, lim_a, scale_log2);
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j) {
+            o[j][0] *= u.alpha;
+            o[j][1] *= u.alpha;
+        }
+        if constexpr (TWO_ROWS) {
+            pa[0] = u.p01;
+            pa[2] = u.p89;
+        } else {
+            pa[0] = u.p01;
+            pa[1] = u.p89;
+        }
+    }
+    if constexpr (TWO_ROWS) {
+        const RowUpdate u = row_update(rs.m_b, rs.l_b, s0[2], s0[3], s1[2], s1[3], t0, lim_b, scale_log2);
+#pragma unroll
+        for (int j = 0; j < D / 8; ++j) {
+            o[j][2] *= u.alpha;
+            o[j][3] *= u.alpha;
+        }
+        pa[1] = u.p01;
+        pa[3] = u.p89;
+    }
+    {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int tok = rr + ((mi & 1) << 3);  // matrices 0,2: tokens 0-7; 1,3: tokens 8-15
+        const int csel = mi >> 1;              // matrices 0,1: even 8-column chunk; 2,3: odd
+        // transposed fragments: b0/b2 hold keys t0 (low half) and t0+1 (high half), b1/b3
+        // keys t0+8 and t0+9; keys at or past vlim are zeroed
+        const uint32_t m0 = vlim >= kBlockSize ? 0xffffffffu
+                                               : (t0 < vlim ? 0x0000ffffu : 0u) | (t0 + 1 < vlim ? 0xffff0000u : 0u);
+        const uint32_t m1 = vlim >= kBlockSize ? 0xffffffffu
+                                               : (t0 + 8 < vlim ? 0x0000ffffu : 0u) | (t0 + 9 < vlim ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int nn = 0; nn < D / 16; ++nn) {
+            const int chunk = nn * 2 + csel;
+            const uint32_t addr = vs + (chunk >> 3) * KvTile<D>::kBoxBytes + swz128(tok, chunk & 7);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(addr, b0, b1, b2, b3);
+            mma_rows<TWO_ROWS>(o[2 * nn], pa, b0 & m0, b1 & m1);
+            mma_rows<TWO_ROWS>(o[2 * nn + 1], pa, b2 & m0, b3 & m1);
+        }
+    }
+}
+
+// Q A-fragments of a 16-row tile from global memory.  row_a / row_b: the rows this
+// thread feeds (lane/4 and lane/4 + 8), nullptr for a padding row.
+template <int D, bool TWO_ROWS>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qa)[D / 16][Rows<TWO_ROWS>::kA], const __nv_bfloat16* row_a,
+                                             const __nv_bfloat16* row_b) {
+    const int c = (threadIdx.x & 3) * 2;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t lo = row_a ? ld_u32(row_a + kk * 16 + c) : 0u;
+        const uint32_t hi = row_a ? ld_u32(row_a + kk * 16 + c + 8) : 0u;
+        if constexpr (TWO_ROWS) {
+            qa[kk][0] = lo;
+            qa[kk][2] = hi;
+            qa[kk][1] = row_b ? ld_u32(row_b + kk * 16 + c) : 0u;
+            qa[kk][3] = row_b ? ld_u32(row_b + kk * 16 + c + 8) : 0u;
+        } else {
+            qa[kk][0] = lo;
+            qa[kk][1] = hi;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+}  // namespace pa

@@ -1,0 +1,62 @@
+// pa_internal.h -- what the C-ABI layer (pa_capi.cu) hands to the kernel launchers.
+// Host-side only; no torch types anywhere in the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+// A validated pool: [num_blocks, num_kv_heads, 16, head_dim] bf16 for K and for V,
+// plus one 2-D TMA map per tensor that views it as [num_blocks*num_kv_heads*16 rows,
+// head_dim] with a 64-element x 16-row box and 128-byte swizzling.
+struct PoolView {
+    void* k;
+    void* v;
+    int num_blocks;
+    int num_kv_heads;
+    int head_dim;
+    CUtensorMap tm_k;
+    CUtensorMap tm_v;
+};
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int max_smem_optin;
+};
+
+// Per-call arguments of the attention kernels (decode, split-KV, prefill).
+struct AttnArgs {
+    const void* q;               // decode [B, Hq, D]; prefill [sum C, Hq, D] bf16
+    const int32_t* block_tables; // [B, max_blocks]
+    const int32_t* seq_lens;     // [B]
+    const int32_t* cu_q_lens;    // prefill only, [B+1]
+    void* out;                   // bf16, same shape as q
+    float* ws_o;                 // split-KV partial outputs [B, Hq, P, D] fp32
+    float* ws_lse;               // split-KV partial log-sum-exp [B, Hq, P] fp32
+    unsigned* status;            // device status word
+    int batch;
+    int num_heads;
+    int max_blocks;
+    int num_partitions;          // split-KV only
+    int max_chunk;               // prefill only
+    float scale;
+};
+
+const DeviceInfo& device_info();
+unsigned* device_status_ptr();
+
+cudaError_t launch_kv_append(const PoolView& pool, const void* k_new, const void* v_new, const int64_t* slots,
+                             int num_tokens, unsigned* status, cudaStream_t stream);
+cudaError_t launch_decode(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_splitkv(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const float* ws_o, const float* ws_lse, int batch, int num_heads, int head_dim,
+                           int num_partitions, void* out, cudaStream_t stream);
+cudaError_t launch_prefill(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
+
+// Split count the decode launcher picks for a problem (exposed for tests and tuning).
+int decode_splits_for(int batch, int num_kv_heads, int max_blocks);
+
+}  // namespace pa

@@ -1,0 +1,244 @@
+"""CUDA path against the fp64 oracle, through the C ABI, on the same seeded inputs.
+
+Covers every call: the append (bit-exact), decode (single CTA and thread-block-cluster
+splits), split-KV partitions and their combine, chunked prefill; the five workloads at
+full size (prefill sampled row by row at full size, whole at reduced size) plus ragged
+sweeps over sequence length, group size, head dim and partition count, the degenerate
+cases (empty sequences, one key, more partitions than blocks), NaN leak sentinels, and
+the device status word for out-of-pool ids.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_gqa_slot_gb300 as pa
+import workloads as W
+import golden_cases as G
+from parity import GpuCase, compare, oracle_pool, oracle_decode, oracle_prefill, check_status_clean
+from workloads import u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    pa.library()
+    pa.pa_device_status(clear=True)
+    yield
+
+
+# ------------------------------------------------------------------ append
+@pytest.mark.parametrize("make", [W.batched_decode, W.chunked_prefill,
+                                  lambda: W.random_case(11, batch=5, num_heads=8, num_kv_heads=2, head_dim=64,
+                                                        prefill=True, q_len=30)],
+                         ids=["batched_decode", "chunked_prefill", "random_d64"])
+def test_kv_append_bit_exact(make):
+    case = make()
+    g = GpuCase(case)
+    k_ref, v_ref = oracle_pool(case)
+    torch.cuda.synchronize()
+    assert np.array_equal(u16(g.k.cpu()), k_ref)
+    assert np.array_equal(u16(g.v.cpu()), v_ref)
+    check_status_clean("append")
+
+
+def test_kv_append_skips_negative_and_flags_out_of_pool():
+    case = W.random_case(12, batch=3, num_heads=4, num_kv_heads=2, head_dim=128, prefill=True, q_len=10)
+    g = GpuCase(case, append=False)
+    slots = case.slot_mapping.clone()
+    slots[0] = -1
+    bad = slots.clone()
+    bad[1] = case.num_blocks * 16 + 3
+    pa.pa_kv_append(g.pool, g.k_new, g.v_new, bad.cuda())
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    # reference: the same scatter with rows 0 and 1 skipped
+    k = u16(case.k_cache).copy()
+    v = u16(case.v_cache).copy()
+    sm = bad.numpy().copy()
+    sm[1] = -1
+    oracle.load().kv_append(k, v, u16(case.k_new), u16(case.v_new), sm)
+    assert np.array_equal(u16(g.k.cpu()), k) and np.array_equal(u16(g.v.cpu()), v)
+
+
+# ------------------------------------------------------------------ decode
+@pytest.mark.parametrize("make", [W.tiny_decode, W.qwen3_4b_decode, W.batched_decode],
+                         ids=["tiny_decode", "qwen3_4b_decode", "batched_decode"])
+def test_decode_workloads(make):
+    case = make()
+    g = GpuCase(case)
+    out = g.decode()
+    compare(out, oracle_decode(case), case.name)
+    check_status_clean(case.name)
+
+
+SWEEP = [(hq, hkv, d) for d in (64, 128) for (hq, hkv) in ((4, 4), (8, 4), (8, 2), (16, 2), (32, 8), (32, 2))]
+
+
+@pytest.mark.parametrize("hq,hkv,d", SWEEP)
+def test_decode_ragged_sweep(hq, hkv, d):
+    for j, (lo, hi) in enumerate(((1, 17), (15, 70), (100, 400))):
+        case = W.random_case(2000 + 31 * hq + hkv + d + j, batch=7, num_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             min_len=lo, max_len=hi)
+        g = GpuCase(case)
+        compare(g.decode(), oracle_decode(case), f"decode {hq}/{hkv}/{d} len {lo}-{hi}")
+    check_status_clean("decode sweep")
+
+
+@pytest.mark.parametrize("L", [1, 15, 16, 17, 33, 64, 255, 256, 257, 1000])
+def test_decode_lengths_single_sequence(L):
+    """One sequence: few CTAs, so the cluster-split path with ragged per-split ranges."""
+    case = W.paged_case(name=f"len{L}", seed=3000 + L, seq_lens=[L], q_lens=[1], new_lens=[1], num_heads=32,
+                        num_kv_heads=8, head_dim=128, num_blocks=max(8, 2 * (L // 16 + 1)))
+    g = GpuCase(case)
+    compare(g.decode(), oracle_decode(case), case.name)
+    check_status_clean(case.name)
+
+
+def test_decode_empty_sequences_give_zero():
+    case = W.paged_case(name="empty", seed=5, seq_lens=[0, 40, 0, 3], q_lens=[1] * 4, new_lens=[0] * 4, num_heads=8,
+                        num_kv_heads=2, head_dim=128, num_blocks=16)
+    g = GpuCase(case)
+    out = g.decode()
+    ref = oracle_decode(case)
+    compare(out, ref, "empty")
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+
+
+@pytest.mark.parametrize("spec", [c for c in G.load_cases() if c["kind"] == "decode"], ids=lambda c: c["name"])
+def test_decode_golden_closed_forms(spec):
+    case = G.build(spec)
+    g = GpuCase(case, append=False)
+    compare(g.decode(), G.expected(spec), spec["name"])
+
+
+def test_decode_flags_out_of_pool_block():
+    case = W.random_case(13, batch=2, num_heads=8, num_kv_heads=2, head_dim=128, min_len=40, max_len=60)
+    g = GpuCase(case)
+    bt = case.block_tables.clone()
+    bt[1, 1] = case.num_blocks + 7
+    pa.pa_decode(g.pool, g.q, bt.cuda(), g.sl, case.scale)
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    # the other sequence is untouched by the bad id
+    out = pa.pa_decode(g.pool, g.q, bt.cuda(), g.sl, case.scale)
+    pa.pa_device_status(clear=True)
+    ref = oracle_decode(case)
+    compare(out[:1], ref[:1], "good sequence next to a bad block id")
+
+
+# ------------------------------------------------------------------ split-KV + combine
+def _check_split(case, P, pool=None):
+    g = GpuCase(case)
+    ws_o, ws_lse = g.splitkv(P)
+    k, v = pool if pool is not None else oracle_pool(case)
+    orc = oracle.load()
+    o_ref, lse_ref = orc.decode_partitions(k, v, u16(case.q), case.block_tables.numpy(), case.seq_lens.numpy(),
+                                           case.scale, P)
+    lse = ws_lse.cpu().double().numpy()
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse), fin), "empty partitions must have lse = -inf"
+    assert np.all(np.isneginf(lse[~fin]))
+    if fin.any():
+        assert np.max(np.abs(lse[fin] - lse_ref[fin])) <= 1e-2
+    compare(ws_o[torch.from_numpy(fin).to(ws_o.device)], o_ref[fin], f"{case.name} P={P} partial O")
+    out = pa.pa_combine(ws_o, ws_lse)
+    compare(out, orc.decode(k, v, u16(case.q), case.block_tables.numpy(), case.seq_lens.numpy(), case.scale),
+            f"{case.name} P={P} combined")
+    check_status_clean(f"split P={P}")
+    return out
+
+
+@pytest.mark.parametrize("P", [8, 16, 32])
+def test_splitkv_4x8192(P):
+    case = W.splitkv_decode(1004, 4, 8192)
+    _check_split(case, P)
+
+
+@pytest.mark.parametrize("P", [8, 32])
+def test_splitkv_1x32768(P):
+    case = W.splitkv_decode(1004, 1, 32768)
+    _check_split(case, P)
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 8, 64])
+def test_splitkv_ragged_and_empty_partitions(P):
+    case = W.random_case(4000 + P, batch=6, num_heads=16, num_kv_heads=2, head_dim=128, min_len=1, max_len=300)
+    _check_split(case, P)
+
+
+def test_splitkv_one_partition_equals_decode():
+    case = W.random_case(4100, batch=4, num_heads=32, num_kv_heads=8, head_dim=128, min_len=50, max_len=200)
+    g = GpuCase(case)
+    dec = g.decode()
+    ws_o, ws_lse = g.splitkv(1)
+    merged = pa.pa_combine(ws_o, ws_lse)
+    assert (merged.float() - dec.float()).abs().max().item() <= 2 ** -7
+
+
+def test_splitkv_golden_partitions():
+    spec = [c for c in G.load_cases() if c["name"] == "three_blocks"][0]
+    case = G.build(spec)
+    g = GpuCase(case, append=False)
+    for P in (2, 3, 4):
+        ws_o, ws_lse = g.splitkv(P)
+        wo, wl = G.expected_partitions(spec, P)
+        fin = np.isfinite(wl)
+        lse = ws_lse[0, 0].cpu().double().numpy()
+        assert np.all(np.isneginf(lse[~fin]))
+        assert np.max(np.abs(lse[fin] - wl[fin])) <= 1e-3
+        assert np.max(np.abs(ws_o[0, 0].cpu().double().numpy() - wo)) <= 1e-3
+        compare(pa.pa_combine(ws_o, ws_lse), G.expected(spec), f"golden P={P}")
+
+
+# ------------------------------------------------------------------ chunked prefill
+def test_prefill_chunked_full_size_sampled_rows():
+    """The full workload (8 x 256-token chunks over a shared 768-token prefix), every
+    chunk position class sampled: first/last query of each chunk and random rows."""
+    case = W.chunked_prefill()
+    g = GpuCase(case)
+    out = g.prefill()
+    check_status_clean("chunked_prefill")
+    k, v = oracle_pool(case)
+    gen = np.random.default_rng(77)
+    T, H = case.q.shape[0], case.num_heads
+    toks = np.concatenate([np.arange(0, T, 256), np.arange(255, T, 256), gen.integers(0, T, 48)]).astype(np.int32)
+    heads = gen.integers(0, H, toks.size).astype(np.int32)
+    ref = oracle.load().prefill_rows(k, v, u16(case.q), case.cu_q_lens.numpy(), case.block_tables.numpy(),
+                                     case.seq_lens.numpy(), case.scale, toks, heads)
+    compare(out[torch.from_numpy(toks).long(), torch.from_numpy(heads).long()], ref, "chunked_prefill rows")
+
+
+def test_prefill_chunked_reduced_whole():
+    case = W.chunked_prefill(seed=1105, batch=3, prefix_blocks=5, chunk=100)
+    g = GpuCase(case)
+    compare(g.prefill(), oracle_prefill(case), "chunked_prefill reduced")
+    check_status_clean("prefill reduced")
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(4, 4, 64), (8, 2, 64), (32, 8, 128), (16, 2, 128), (12, 4, 128), (64, 8, 128)])
+def test_prefill_ragged_sweep(hq, hkv, d):
+    for j, shared in enumerate((0, 32)):
+        case = W.random_case(5000 + hq * 7 + hkv + d + j, batch=4, num_heads=hq, num_kv_heads=hkv, head_dim=d,
+                             min_len=1 + shared, max_len=200, q_len=70, prefill=True, shared_prefix_tokens=shared)
+        g = GpuCase(case)
+        compare(g.prefill(), oracle_prefill(case), f"prefill {hq}/{hkv}/{d} shared {shared}")
+    check_status_clean("prefill sweep")
+
+
+def test_prefill_one_row_chunk_equals_decode():
+    case = W.random_case(5100, batch=5, num_heads=32, num_kv_heads=8, head_dim=128, min_len=20, max_len=300)
+    g = GpuCase(case)
+    dec = g.decode()
+    cu = torch.arange(case.batch + 1, dtype=torch.int32, device="cuda")
+    pre = pa.pa_prefill_chunked(g.pool, g.q, cu, g.bt, g.sl, case.scale, 1)
+    # same arithmetic order is not required; both must be within tolerance of the oracle
+    ref = oracle_decode(case)
+    compare(dec, ref, "decode")
+    compare(pre, ref, "one-row prefill")
+
+
+def test_prefill_golden_causal_chunk():
+    spec = [c for c in G.load_cases() if c["kind"] == "prefill"][0]
+    case = G.build(spec)
+    g = GpuCase(case, append=False)
+    compare(g.prefill(), G.expected(spec), spec["name"])
