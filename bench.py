@@ -1,0 +1,597 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged GQA attention hot path (libpagedattn) on GB300.
+
+One step = one pass of every call of the hot path over its workload, inputs resident
+in HBM:
+  1. pa_kv_append        64 new tokens            (batched decode: 64 seqs, ctx ~U[1024,1152], 32q/8kv/128)
+  2. pa_decode           batched decode, 64 seqs  (same)
+  3. pa_decode_splitkv   4 x 8192, P=8  + pa_combine   (Qwen3-32B-shaped 64q/8kv/128)
+  4. pa_decode_splitkv   1 x 32768, P=32 + pa_combine
+  5. pa_kv_append        8 x 256 chunk tokens     (chunked prefill over a shared 768-token prefix)
+  6. pa_prefill_chunked  8 x 256-token causal chunks, 32q/8kv/128
+value = KV bytes the attention calls must read per step / step time (GB/s), L2 flushed
+(a 512 MB buffer is read) before every timed step.  Each call is also timed on its own
+stream with CUDA events and reported under "per_call".  The two latency-bound decode
+shapes (1 seq x 37 tokens, 4q/1kv/64; 1 seq x 1152 tokens, 32q/8kv/128) are reported
+under "latency" (cold and CUDA-graph-replayed).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU fp64 oracle (the reference arm of this comparison) on a
+bounded sample of the same step.  Under torchrun (N > 1) every rank runs the full step on
+its own GPU (independent replicas, weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "paged GQA decode: KV GB/s & frac of GB300 HBM peak; µs/call per batch×ctx"
+WORKLOAD = ("serving step: append(64) + decode 64x~1088 (32q/8kv/128) + split-KV 4x8192 and 1x32768 (P in 8..32) "
+            "with combine (64q/8kv/128) + append(2048) + chunked prefill 8x256 over a shared 768-token "
+            "prefix (32q/8kv/128); block 16; bf16 N(0,1)")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = {
+    "decode": ["pa_decode.cu", "pa_block_attn.cuh", "pa_device.cuh"],
+    "splitkv": ["pa_decode.cu", "pa_block_attn.cuh", "pa_device.cuh"],
+    "prefill": ["pa_prefill.cu", "pa_block_attn.cuh", "pa_device.cuh"],
+    "append": ["pa_append.cu", "pa_device.cuh"],
+    "combine": ["pa_decode.cu", "pa_device.cuh"],
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------- peaks, clocks, profiles
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        h.update((ROOT / "paged_kv_gqa_slot_gb300" / "csrc" / f).read_bytes())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if its sources still match."""
+    pat = re.compile(r"^traffic:\s+kernel=(\S+)\s+workload=(\S+)\s+dram_bytes_per_launch=(\d+)\s+source_sha=(\S+)")
+    for f in sorted((ROOT / "profiles").glob("*.md")):
+        for line in f.read_text().splitlines():
+            m = pat.match(line.strip())
+            if m and m.group(1) == kind and m.group(2) == workload:
+                return int(m.group(3)) if m.group(4) == source_sha(kind) else None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is under load."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(ROOT / "gpurun_out" / f".clocks_{os.getpid()}.csv", "w") if (ROOT / "gpurun_out").exists() \
+                else open(f"/tmp/.clocks_{os.getpid()}.csv", "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        for line in Path(self.out.name).read_text().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        try:
+            os.unlink(self.out.name)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- workload
+def causal_flops(case) -> float:
+    """QK^T and PV multiply-adds of the chunked prefill, causal-exact (2 flops each)."""
+    keys = 0
+    for L, C in zip(case.seq_lens.tolist(), case.q_lens):
+        pre = L - C
+        keys += C * pre + C * (C + 1) // 2
+    return float(keys) * case.num_heads * case.head_dim * 4
+
+
+def attn_bytes(case, extra_q_out=True) -> int:
+    """Algorithmic bytes of one attention call: K and V once per kv head, plus q and out."""
+    b = case.kv_bytes()
+    if extra_q_out:
+        b += 2 * case.q.numel() * 2
+    return b
+
+
+class Step:
+    """Device-resident inputs of one step and the calls that make it."""
+
+    GROUPS = {"decode": ("c3",), "splitkv": ("c4a", "c4b"), "prefill": ("c5",), "tiny_decode": ("c1",),
+              "qwen3_4b_decode": ("c2",)}
+
+    def __init__(self, device, only=None):
+        import paged_kv_gqa_slot_gb300 as pa
+        import workloads as W
+        self.pa = pa
+        groups = set(self.GROUPS[only]) if only else {"c3", "c4a", "c4b", "c5"}
+        t0 = time.time()
+        self.c1 = W.tiny_decode() if "c1" in groups else None
+        self.c2 = W.qwen3_4b_decode() if "c2" in groups else None
+        self.c3 = W.batched_decode() if "c3" in groups else None
+        self.c4a = W.splitkv_decode(1004, 4, 8192) if "c4a" in groups else None
+        self.c4b = W.splitkv_decode(1004, 1, 32768) if "c4b" in groups else None
+        self.c5 = W.chunked_prefill() if "c5" in groups else None
+        log(f"[bench] workloads drawn in {time.time() - t0:.1f}s")
+        self.dev = device
+        d = device
+
+        def up(c):
+            if c is None:
+                return None
+            g = {"k": c.k_cache.to(d), "v": c.v_cache.to(d), "q": c.q.to(d), "bt": c.block_tables.to(d),
+                 "sl": c.seq_lens.to(d), "cu": c.cu_q_lens.to(d), "k_new": c.k_new.to(d),
+                 "v_new": c.v_new.to(d), "slots": c.slot_mapping.to(d)}
+            g["pool"] = pa.PaPool(g["k"], g["v"])
+            g["out"] = torch.empty_like(g["q"])
+            return g
+
+        self.g1, self.g2 = up(self.c1), up(self.c2)
+        self.g3, self.g4a, self.g4b, self.g5 = up(self.c3), up(self.c4a), up(self.c4b), up(self.c5)
+        # partitions as the library suggests, kept within the workload's 8..32
+        self.P4a = min(32, max(8, pa.pa_splitkv_num_partitions(4, 8, 512))) if self.c4a is not None else 8
+        self.P4b = min(32, max(8, pa.pa_splitkv_num_partitions(1, 8, 2048))) if self.c4b is not None else 32
+        for g, c, P in ((self.g4a, self.c4a, self.P4a), (self.g4b, self.c4b, self.P4b)):
+            if g is None:
+                continue
+            g["ws_o"] = torch.empty((c.batch, c.num_heads, P, c.head_dim), dtype=torch.float32, device=d)
+            g["ws_lse"] = torch.empty((c.batch, c.num_heads, P), dtype=torch.float32, device=d)
+        c3, c4a, c4b, c5 = self.c3, self.c4a, self.c4b, self.c5
+        g3, g4a, g4b, g5 = self.g3, self.g4a, self.g4b, self.g5
+        app_bytes = lambda c: 2 * 2 * c.k_new.numel() * 2  # read new rows, write pool rows, K and V
+        ws_bytes = lambda g: g["ws_o"].numel() * 4 + g["ws_lse"].numel() * 4 + g["out"].numel() * 2
+        # (name, kind, fn, units, unit_kind)
+        self.calls = []
+        for g, c, nm in ((self.g1, self.c1, "decode[tiny,1x37,4q/1kv/64]"),
+                         (self.g2, self.c2, "decode[qwen3_4b,1x1152,32q/8kv/128]")):
+            if g is not None:
+                self.calls.append((nm, "decode", (lambda g=g, c=c: pa.pa_decode(g["pool"], g["q"], g["bt"], g["sl"],
+                                                                               c.scale, g["out"])),
+                                   attn_bytes(c), "bytes"))
+        if g3 is not None:
+            self.calls += [
+                ("kv_append[batched_decode,64]", "append",
+                 lambda: pa.pa_kv_append(g3["pool"], g3["k_new"], g3["v_new"], g3["slots"]), app_bytes(c3), "bytes"),
+                ("decode[batched_decode,64x~1088]", "decode",
+                 lambda: pa.pa_decode(g3["pool"], g3["q"], g3["bt"], g3["sl"], c3.scale, g3["out"]),
+                 attn_bytes(c3), "bytes")]
+        if g4a is not None:
+            self.calls += [
+                (f"decode_splitkv[4x8192,P={self.P4a}]", "splitkv",
+                 lambda: pa.pa_decode_splitkv(g4a["pool"], g4a["q"], g4a["bt"], g4a["sl"], c4a.scale, self.P4a,
+                                              g4a["ws_o"], g4a["ws_lse"]), attn_bytes(c4a), "bytes"),
+                (f"combine[4x8192,P={self.P4a}]", "combine", lambda: pa.pa_combine(g4a["ws_o"], g4a["ws_lse"], g4a["out"]),
+                 ws_bytes(g4a), "bytes")]
+        if g4b is not None:
+            self.calls += [
+                (f"decode_splitkv[1x32768,P={self.P4b}]", "splitkv",
+                 lambda: pa.pa_decode_splitkv(g4b["pool"], g4b["q"], g4b["bt"], g4b["sl"], c4b.scale, self.P4b,
+                                              g4b["ws_o"], g4b["ws_lse"]), attn_bytes(c4b), "bytes"),
+                (f"combine[1x32768,P={self.P4b}]", "combine", lambda: pa.pa_combine(g4b["ws_o"], g4b["ws_lse"], g4b["out"]),
+                 ws_bytes(g4b), "bytes")]
+        if g5 is not None:
+            mx5 = max(c5.q_lens)
+            self.calls += [
+                ("kv_append[chunked_prefill,2048]", "append",
+                 lambda: pa.pa_kv_append(g5["pool"], g5["k_new"], g5["v_new"], g5["slots"]), app_bytes(c5), "bytes"),
+                ("prefill_chunked[8x256 over 768]", "prefill",
+                 lambda: pa.pa_prefill_chunked(g5["pool"], g5["q"], g5["cu"], g5["bt"], g5["sl"], c5.scale, mx5,
+                                               g5["out"]), causal_flops(c5), "flops")]
+        # the step's metric: KV bytes the attention calls must read
+        cases = ((self.g1, self.c1), (self.g2, self.c2), (g3, c3), (g4a, c4a), (g4b, c4b), (g5, c5))
+        self.step_kv_bytes = sum(c.kv_bytes() for _, c in cases if c is not None)
+        self.cases = [(g, c) for g, c in cases if c is not None]
+
+    def run(self, events=None):
+        for i, (_, _, fn, _, _) in enumerate(self.calls):
+            fn()
+            if events is not None:
+                events[i + 1].record()
+
+    # ---- end-to-end: inputs from pinned host memory, outputs back to pinned host memory
+    def e2e_setup(self):
+        d = self.dev
+        self.h2d = []  # (host pinned, device)
+        for g, c in self.cases:
+            for key, src in (("q", c.q), ("bt", c.block_tables), ("sl", c.seq_lens), ("cu", c.cu_q_lens),
+                             ("k_new", c.k_new), ("v_new", c.v_new), ("slots", c.slot_mapping)):
+                if src.numel() == 0:
+                    continue
+                self.h2d.append((src.contiguous().pin_memory(), g[key]))
+        self.d2h = [(torch.empty_like(g["out"], device="cpu").pin_memory(), g["out"]) for g, _ in self.cases]
+        self.h2d_bytes = sum(h.numel() * h.element_size() for h, _ in self.h2d)
+        self.d2h_bytes = sum(h.numel() * h.element_size() for h, _ in self.d2h)
+
+    def e2e_run(self):
+        for h, dv in self.h2d:
+            dv.copy_(h, non_blocking=True)
+        self.run()
+        for h, dv in self.d2h:
+            h.copy_(dv, non_blocking=True)
+
+
+def call_workload(name: str) -> str:
+    """Workload label of a call, as used by the traffic lines of the profile summaries."""
+    for key, label in (("tiny", "tiny_decode"), ("qwen3_4b", "qwen3_4b_decode"), ("batched", "batched_decode"),
+                       ("4x8192", "splitkv_4x8192"), ("1x32768", "splitkv_1x32768"), ("chunked", "chunked_prefill"),
+                       ("8x256", "chunked_prefill")):
+        if key in name:
+            return label
+    return "unknown"
+
+
+def flush_l2(buf):
+    # reading a buffer larger than L2 leaves it full of clean lines of that buffer
+    return buf.sum()
+
+
+def time_steps(step, steps, warmup, flush_buf):
+    n = len(step.calls)
+    for _ in range(warmup):
+        flush_l2(flush_buf)
+        step.run()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
+    for k in range(steps):
+        flush_l2(flush_buf)
+        evs[k][0].record()
+        step.run(evs[k])
+    torch.cuda.synchronize()
+    per_call = np.zeros((steps, n))
+    for k in range(steps):
+        for i in range(n):
+            per_call[k, i] = evs[k][i].elapsed_time(evs[k][i + 1]) * 1e3  # us
+    return per_call
+
+
+def time_e2e(step, steps, flush_buf):
+    step.e2e_setup()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(2):  # warm the copies
+        step.e2e_run()
+    torch.cuda.synchronize()
+    for _ in range(steps):
+        flush_l2(flush_buf)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        step.e2e_run()
+        e.record()
+        e.synchronize()
+        ts.append(s.elapsed_time(e) * 1e3)
+    return float(np.mean(ts))
+
+
+def latency_configs(flush_buf):
+    import paged_kv_gqa_slot_gb300 as pa
+    import workloads as W
+    res = {}
+    for name, make in (("tiny_decode[1x37,4q/1kv/64]", W.tiny_decode),
+                       ("qwen3_4b_decode[1x1152,32q/8kv/128]", W.qwen3_4b_decode)):
+        c = make()
+        k, v = c.k_cache.cuda(), c.v_cache.cuda()
+        pool = pa.PaPool(k, v)
+        q, bt, sl = c.q.cuda(), c.block_tables.cuda(), c.seq_lens.cuda()
+        out = torch.empty_like(q)
+        fn = lambda: pa.pa_decode(pool, q, bt, sl, c.scale, out)
+        for _ in range(5):
+            fn()
+        cold = []
+        for _ in range(30):
+            flush_l2(flush_buf)
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            e.synchronize()
+            cold.append(s.elapsed_time(e) * 1e3)
+        # warm: 100 calls replayed from one CUDA graph
+        st = torch.cuda.Stream()
+        st.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(st):
+            fn()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(graph, stream=st):
+                for _ in range(100):
+                    fn()
+        torch.cuda.current_stream().wait_stream(st)
+        graph.replay()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        for _ in range(5):
+            graph.replay()
+        e.record()
+        e.synchronize()
+        warm = s.elapsed_time(e) * 1e3 / 500
+        kvb = attn_bytes(c)
+        res[name] = {"us_per_call_cold": round(float(np.median(cold)), 2), "us_per_call_graph_warm": round(warm, 2),
+                     "kv_gbs_cold": round(kvb / float(np.median(cold)) / 1e3, 1),
+                     "decode_splits": pa.pa_decode_num_splits(c.batch, c.num_kv_heads, c.max_blocks)}
+        del graph
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle baseline
+class OracleSample:
+    """A bounded sample of the step for the fp64 CPU oracle: the decode and split-KV calls
+    whole, the chunked prefill on every `prefill_stride`-th (token, head) row."""
+
+    def __init__(self, prefill_stride=16, decode_seqs=None):
+        import oracle
+        import workloads as W
+        from workloads import u16
+        self.orc = oracle.load()
+        self.u16 = u16
+        self.c3 = W.batched_decode()
+        if decode_seqs is not None:
+            self.c3 = self._first_seqs(self.c3, decode_seqs)
+        self.c4a = W.splitkv_decode(1004, 4, 8192)
+        self.c4b = W.splitkv_decode(1004, 1, 32768)
+        self.c5 = W.chunked_prefill()
+        T, H = self.c5.q.shape[0], self.c5.num_heads
+        idx = np.arange(0, T * H, prefill_stride)
+        self.rows_t = (idx // H).astype(np.int32)
+        self.rows_h = (idx % H).astype(np.int32)
+        self.prefill_frac = len(idx) / (T * H)
+        self.kv_bytes = (self.c3.kv_bytes() + self.c4a.kv_bytes() + self.c4b.kv_bytes()
+                         + self.c5.kv_bytes() * self.prefill_frac)
+        self.pools = {}
+        for name, c in (("c3", self.c3), ("c4a", self.c4a), ("c4b", self.c4b), ("c5", self.c5)):
+            k, v = u16(c.k_cache).copy(), u16(c.v_cache).copy()
+            self.pools[name] = (k, v)
+
+    @staticmethod
+    def _first_seqs(c, n):
+        """The first n sequences of a decode case (one appended token per sequence)."""
+        import workloads as W
+        return W.PagedCase(**{**c.__dict__, "q": c.q[:n], "block_tables": c.block_tables[:n],
+                              "seq_lens": c.seq_lens[:n], "q_lens": c.q_lens[:n], "cu_q_lens": c.cu_q_lens[:n + 1],
+                              "k_new": c.k_new[:n], "v_new": c.v_new[:n], "slot_mapping": c.slot_mapping[:n],
+                              "k_seq": c.k_seq[:n], "v_seq": c.v_seq[:n]})
+
+    def run(self):
+        o, u16 = self.orc, self.u16
+        k, v = self.pools["c3"]
+        c = self.c3
+        o.kv_append(k, v, u16(c.k_new), u16(c.v_new), c.slot_mapping.numpy())
+        o.decode(k, v, u16(c.q), c.block_tables.numpy(), c.seq_lens.numpy(), c.scale)
+        for name, c, P in (("c4a", self.c4a, 8), ("c4b", self.c4b, 32)):
+            k, v = self.pools[name]
+            op, lse = o.decode_partitions(k, v, u16(c.q), c.block_tables.numpy(), c.seq_lens.numpy(), c.scale, P)
+            o.combine(op, lse)
+        k, v = self.pools["c5"]
+        c = self.c5
+        o.kv_append(k, v, u16(c.k_new), u16(c.v_new), c.slot_mapping.numpy())
+        o.prefill_rows(k, v, u16(c.q), c.cu_q_lens.numpy(), c.block_tables.numpy(), c.seq_lens.numpy(), c.scale,
+                       self.rows_t, self.rows_h)
+
+
+def describe_sample(s: OracleSample) -> str:
+    return (f"append + decode of {s.c3.batch} batched-decode sequences, split-KV 4x8192 (P=8) and 1x32768 (P=32) "
+            f"with combine, append + chunked prefill on {s.prefill_frac:.4f} of its (token, head) rows; "
+            f"{s.kv_bytes / 1e6:.1f} MB of KV-equivalent work")
+
+
+# ----------------------------------------------------------------------------- main
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def base_config():
+    return {"workload": WORKLOAD, "l2": "flushed before every timed step (512 MB buffer read)",
+            "timing": "CUDA events on the launching stream around every call; step = sum"}
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    sample = OracleSample(prefill_stride=64, decode_seqs=16)
+    for _ in range(args.warmup):
+        sample.run()
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        sample.run()
+        ts.append(time.perf_counter() - t0)
+    mean_s = float(np.mean(ts))
+    value = sample.kv_bytes / mean_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_s * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": base_config(),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": describe_sample(sample)},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=sorted(Step.GROUPS),
+                    help="time only this part of the step (for profiling); skips the extras")
+    args = ap.parse_args(argv)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_gqa_slot_gb300 as pa
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    peaks, peak_src = load_peaks()
+    step = Step(dev, args.only)
+    extras = args.only is None
+    flush_buf = torch.ones(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    pa.pa_device_status(clear=True)
+
+    # clocks are sampled over a sustained stretch of steps and the timed steps
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    t_end = time.time() + (1.5 if extras else 0.0)
+    while time.time() < t_end:
+        flush_l2(flush_buf)
+        step.run()
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    per_call = time_steps(step, args.steps, args.warmup, flush_buf)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    wall = time.time() - wall0
+    clocks = sampler.stop()
+    status = pa.pa_device_status(clear=True)
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the timed steps")
+
+    step_us = per_call.sum(axis=1)
+    mean_step_us = float(step_us.mean())
+    if ws > 1:
+        t = torch.tensor([mean_step_us], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        mean_step_us = float(t.item())
+    value = ws * step.step_kv_bytes / mean_step_us / 1e3  # GB/s
+
+    # per call
+    calls = {}
+    means = per_call.mean(axis=0)
+    for (name, kind, _, units, ukind), us in zip(step.calls, means):
+        if ukind == "bytes":
+            ach = units / us / 1e3
+            calls[name] = {"us": round(float(us), 2), "GB/s": round(ach, 1),
+                           "frac_hbm": round(ach / peaks["hbm_gbs"], 3), "share": round(float(us) / means.sum(), 3)}
+        else:
+            ach = units / us / 1e6
+            calls[name] = {"us": round(float(us), 2), "TFLOP/s": round(ach, 1),
+                           "frac_bf16": round(ach / peaks["bf16_tflops"], 3), "share": round(float(us) / means.sum(), 3)}
+    # dominant kernel of the step
+    di = int(np.argmax(means))
+    dname, dkind, _, dunits, dukind = step.calls[di]
+    wl = call_workload(dname)
+    if dukind == "bytes":
+        ach = dunits / means[di] / 1e3
+        roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 3), "traffic": profiled_traffic(dkind, wl),
+                "algorithmic_bytes_per_launch": int(dunits), "peak_source": peak_src}
+    else:
+        ach = dunits / means[di] / 1e6
+        roof = {"kernel": dname, "bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 3), "traffic": profiled_traffic(dkind, wl),
+                "algorithmic_flops_per_launch": int(dunits), "peak_source": peak_src}
+
+    # end to end through the public API with host buffers
+    e2e, lat = None, {}
+    if extras:
+        e2e_us = time_e2e(step, max(5, min(args.steps, 20)), flush_buf)
+        e2e = {"value": round(step.step_kv_bytes / e2e_us / 1e3, 1), "unit": "GB/s",
+               "h2d_bytes_per_step": int(step.h2d_bytes), "d2h_bytes_per_step": int(step.d2h_bytes)}
+        lat = latency_configs(flush_buf) if rank == 0 else {}
+
+    cpu = None
+    if rank == 0 and ws == 1 and extras and not args.no_cpu_baseline:
+        sample = OracleSample(prefill_stride=4)
+        t0 = time.perf_counter()
+        sample.run()
+        dt = time.perf_counter() - t0
+        cpu = {"value": round(sample.kv_bytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": describe_sample(sample) + f"; {dt:.1f}s single-threaded on the host"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(mean_step_us / 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": base_config() if extras else {**base_config(), "workload": f"only {args.only}"},
+            "step_kv_bytes": int(step.step_kv_bytes),
+            "roofline": roof, "per_call": calls, "latency": lat, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": len(step.calls) * args.steps, "clocks": clocks,
+            "wall_s_timed": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

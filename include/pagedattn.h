@@ -159,6 +159,12 @@ int pa_device_status(uint32_t *flags, int32_t clear, pa_stream_t stream);
 /* Number of cluster splits pa_decode uses for this shape on the current device. */
 int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
 
+/*
+ * Partition count suggested for pa_decode_splitkv on the current device: a power of two
+ * (1..64) that fills one wave of the GPU's SMs while keeping >= 8 blocks per partition.
+ */
+int pa_splitkv_num_partitions(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
+
 /* Human-readable name of a status code (static string). */
 const char *pa_status_str(int status);
 

@@ -21,15 +21,16 @@ from typing import Optional, Tuple
 import torch
 
 __all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_decode_splitkv", "pa_combine", "pa_prefill_chunked",
-           "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "PagedAttnError",
+           "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "pa_splitkv_num_partitions",
+           "PagedAttnError",
            "library", "library_path", "BLOCK_SIZE", "EXPORTED_SYMBOLS"]
 
 BLOCK_SIZE = 16
 PKG = Path(__file__).resolve().parent
 _LIB_PATH = PKG / "libpagedattn.so"
 EXPORTED_SYMBOLS = ("pa_kv_append", "pa_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv", "pa_combine",
-                    "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_status_str",
-                    "pa_version")
+                    "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_splitkv_num_partitions",
+                    "pa_status_str", "pa_version")
 
 PA_OK = 0
 PA_ERR_INVALID_ARG = -1
@@ -79,6 +80,7 @@ def library() -> ctypes.CDLL:
         "pa_prefill_chunked": (ctypes.c_int, [pool, P, P, P, I32, P, I32, I32, I32, F32, P, P]),
         "pa_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32, P]),
         "pa_decode_num_splits": (ctypes.c_int, [I32, I32, I32]),
+        "pa_splitkv_num_partitions": (ctypes.c_int, [I32, I32, I32]),
         "pa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "pa_version": (ctypes.c_int, []),
     }
@@ -214,6 +216,10 @@ def pa_device_status(clear: bool = True, stream=None) -> int:
 
 def pa_decode_num_splits(batch: int, num_kv_heads: int, max_blocks: int) -> int:
     return int(library().pa_decode_num_splits(batch, num_kv_heads, max_blocks))
+
+
+def pa_splitkv_num_partitions(batch: int, num_kv_heads: int, max_blocks: int) -> int:
+    return int(library().pa_splitkv_num_partitions(batch, num_kv_heads, max_blocks))
 
 
 def default_scale(head_dim: int) -> float:

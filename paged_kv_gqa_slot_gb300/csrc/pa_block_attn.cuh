@@ -2,11 +2,14 @@
 // warp-MMA prefill kernels.
 //
 // Producer: one warp walks a sequence's block table (32 entries per coalesced load,
-// the next 32 prefetched) and, for each logical block, has one lane issue TMA loads of
-// the (block, kv head) K tile and V tile into a ring slot of shared memory.  Each tile
-// is [16 tokens x D] bf16 = one contiguous 2 or 4 KB run of the pool, loaded as D/64
-// boxes of 16 rows x 128 B with 128-byte swizzling.  The block id is only a row
-// coordinate of the tensor map, so paging costs nothing beyond the table read.
+// the next 32 prefetched) and, for each logical block, has two lanes issue the TMA loads
+// of the (block, kv head) K tile and V tile into a ring slot of shared memory.  Each tile
+// is [16 tokens x D] bf16 = one contiguous 2 or 4 KB run of the pool, loaded as ONE box
+// through a 4-D map whose 64-column halves are a dimension of their own (stride 128 B),
+// so it lands half-major ([half][16 rows][128 B], 128-byte swizzled).  Per-box cost, not
+// bytes, limits a TMA stream of small boxes, so one box per tile rather than one per half
+// doubles the rate an SM can pull paged blocks.  The block id is only a coordinate of the
+// tensor map, so paging costs nothing beyond the table read.
 //
 // Consumer: a warp owns a 16-row tile of (query, head) rows.  Per 16-token block it
 // computes S = Q K^T with mma.m16n8k16 (Q fragments stay in registers), masks, updates
@@ -27,10 +30,10 @@ struct KvTile {
 };
 
 // Issue the TMA loads of logical blocks [blk0, blk0 + n) of one sequence into a ring of
-// kStages slots.  Called by a whole warp; returns false if a wait timed out.  On return
+// `stages` slots.  Called by a whole warp; returns false if a wait timed out.  On return
 // every copy it issued has landed (or the wait for it timed out), so the caller may exit.
-template <int D, int kStages>
-__device__ __forceinline__ bool produce_kv_blocks(uint8_t* ring, uint64_t* full, uint64_t* empty,
+template <int D>
+__device__ __forceinline__ bool produce_kv_blocks(uint8_t* ring, int stages, uint64_t* full, uint64_t* empty,
                                                   const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                                   const int32_t* bt, int n, int num_blocks, int num_kv_heads,
                                                   int kvh, unsigned* status, uint64_t policy) {
@@ -50,30 +53,24 @@ __device__ __forceinline__ bool produce_kv_blocks(uint8_t* ring, uint64_t* full,
         for (int j = 0; j < cnt; ++j) {
             const int blk = __shfl_sync(0xffffffffu, cur, j);
             const int i = c0 + j;
-            const int st = i % kStages;
+            const int st = i % stages;
             if (lane == 0) {
-                if (i >= kStages) ok = mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1);
-                if (ok) {
-                    mbar_arrive_expect_tx(&full[st], T::kStageBytes);
-                    const int row = (blk * num_kv_heads + kvh) * kBlockSize;
-                    uint8_t* kd = ring + st * T::kStageBytes;
-                    uint8_t* vd = kd + T::kTileBytes;
-#pragma unroll
-                    for (int h = 0; h < T::kHalves; ++h) {
-                        tma_load_2d(kd + h * T::kBoxBytes, tm_k, h * 64, row, &full[st], policy);
-                        tma_load_2d(vd + h * T::kBoxBytes, tm_v, h * 64, row, &full[st], policy);
-                    }
-                    ++issued;
-                }
+                if (i >= stages) ok = mbar_wait(&empty[st], ((i / stages) & 1) ^ 1);
+                if (ok) mbar_arrive_expect_tx(&full[st], T::kStageBytes);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
             if (!ok) break;
+            // the K and V boxes of the block go out from lanes 0 and 1 in one instruction
+            if (lane < 2)
+                tma_load_tile(ring + st * T::kStageBytes + lane * T::kTileBytes, lane == 0 ? tm_k : tm_v,
+                              blk * num_kv_heads + kvh, &full[st], policy);
+            ++issued;
         }
     }
     // every copy this warp issued must have landed before the CTA may leave
     if (lane == 0) {
-        for (int i = max(0, issued - kStages); i < issued; ++i)
-            if (!mbar_wait(&full[i % kStages], (i / kStages) & 1)) ok = false;
+        for (int i = max(0, issued - stages); i < issued; ++i)
+            if (!mbar_wait(&full[i % stages], (i / stages) & 1)) ok = false;
         if (!ok) atomicOr(status, kDevTimeout);
     }
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
@@ -250,6 +247,124 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qa)[D / 16][Rows<TWO_ROW
             qa[kk][0] = lo;
             qa[kk][1] = hi;
         }
+    }
+}
+
+// ------------------------------------------------------------------------------------
+// Decode form: the query heads of one kv group are the MMA's N dimension (8 per n-tile),
+// the block's 16 tokens (for S^T = K Q^T) and head_dim (for O^T = V^T P^T) are its M
+// dimension, so a block costs 2 * D/16 MMAs per 8 heads with no padding rows.  Each
+// thread holds, per n-tile, heads nt*8 + 2*(lane%4) (+1) for tokens lane/4 and lane/4+8.
+// The P^T accumulator fragment becomes the B operand of the P V product through two
+// in-register 8x8 transposes (movmatrix).
+
+// Per-thread softmax state of its two heads (hA = 2*(lane%4), hB = hA + 1) per n-tile.
+template <int NT>
+struct HeadState {
+    float m[NT][2], l[NT][2];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) m[t][0] = m[t][1] = -INFINITY, l[t][0] = l[t][1] = 0.f;
+    }
+};
+
+// Q as B fragments: qb[nt][kk] = {Q[h][kk*16 + 2t], +1}, {Q[h][kk*16 + 8 + 2t], +1} with
+// h = nt*8 + lane/4; rows >= g (nullptr) are zero.
+template <int D, int NT>
+__device__ __forceinline__ void load_q_heads(uint32_t (&qb)[NT][D / 16][2], const __nv_bfloat16* qg, int g) {
+    const int lane = threadIdx.x & 31, c = (lane & 3) * 2;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int h = nt * 8 + (lane >> 2);
+        const __nv_bfloat16* row = h < g ? qg + (size_t)h * D : nullptr;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qb[nt][kk][0] = row ? ld_u32(row + kk * 16 + c) : 0u;
+            qb[nt][kk][1] = row ? ld_u32(row + kk * 16 + c + 8) : 0u;
+        }
+    }
+}
+
+// One head column's update from this thread's two tokens (x0: token lane/4, x8: lane/4+8);
+// returns alpha and writes the two probabilities back into x0, x8.
+__device__ __forceinline__ float head_update(float& m, float& l, float& x0, float& x8) {
+    float mx = fmaxf(x0, x8);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(m, mx);
+    const float base = mn == -INFINITY ? 0.f : mn;
+    const float alpha = fast_exp2(m - base);
+    x0 = fast_exp2(x0 - base);
+    x8 = fast_exp2(x8 - base);
+    l = l * alpha + (x0 + x8);
+    m = mn;
+    return alpha;
+}
+
+// One 16-token block for all g <= 8*NT heads of a kv group.
+//   ot[nt][mt][4]: O^T accumulators, d = mt*16 + lane/4 (+8), head nt*8 + 2*(lane%4) (+1)
+//   valid        : keys with in-block index < valid exist (the rest are masked and their
+//                  V rows zeroed in the fragments, whatever the slot holds)
+template <int D, int NT>
+__device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const uint32_t (&qb)[NT][D / 16][2],
+                                                 float (&ot)[NT][D / 16][4], HeadState<NT>& hs, int valid,
+                                                 float scale_log2) {
+    const int lane = threadIdx.x & 31;
+    const int mi = lane >> 3, rr = lane & 7;
+    const int ltok = rr + ((mi & 1) << 3);  // K matrices 0,2: tokens 0-7; 1,3: tokens 8-15
+    const int lcs = mi >> 1;                // K matrices 0,1: even d-chunk; 2,3: odd
+    float st[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) st[nt][0] = st[nt][1] = st[nt][2] = st[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const int chunk = kk * 2 + lcs;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(ks + (chunk >> 3) * KvTile<D>::kBoxBytes + swz128(ltok, chunk & 7), a0, a1, a2, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(st[nt], a0, a1, a2, a3, qb[nt][kk][0], qb[nt][kk][1]);
+    }
+    const int t0 = lane >> 2;  // this thread's tokens: t0 and t0 + 8
+    const bool v0 = t0 < valid, v8 = t0 + 8 < valid;
+    uint32_t pb[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        float xa0 = v0 ? st[nt][0] * scale_log2 : -INFINITY, xa8 = v8 ? st[nt][2] * scale_log2 : -INFINITY;
+        float xb0 = v0 ? st[nt][1] * scale_log2 : -INFINITY, xb8 = v8 ? st[nt][3] * scale_log2 : -INFINITY;
+        const float aa = head_update(hs.m[nt][0], hs.l[nt][0], xa0, xa8);
+        const float ab = head_update(hs.m[nt][1], hs.l[nt][1], xb0, xb8);
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+            ot[nt][mt][0] *= aa;
+            ot[nt][mt][2] *= aa;
+            ot[nt][mt][1] *= ab;
+            ot[nt][mt][3] *= ab;
+        }
+        // P^T rows (tokens) t0 / t0+8, columns (heads) 2t, 2t+1 -> transposed: the B operand
+        pb[nt][0] = movmatrix_t(pack_bf16x2(xa0, xb0));
+        pb[nt][1] = movmatrix_t(pack_bf16x2(xa8, xb8));
+    }
+    // V^T A fragments (ldmatrix.trans): matrices 0,1: tokens 0-7, 2,3: tokens 8-15;
+    // 0,2: even d-chunk, 1,3: odd.  a0/a1 hold keys 2t, 2t+1; a2/a3 keys 2t+8, 2t+9.
+    const int vtok = rr + ((mi >> 1) << 3);
+    const int vcs = mi & 1;
+    const int tk = (lane & 3) * 2;
+    const uint32_t m0 = valid >= kBlockSize ? 0xffffffffu
+                                            : (tk < valid ? 0x0000ffffu : 0u) | (tk + 1 < valid ? 0xffff0000u : 0u);
+    const uint32_t m8 = valid >= kBlockSize ? 0xffffffffu
+                                            : (tk + 8 < valid ? 0x0000ffffu : 0u) | (tk + 9 < valid ? 0xffff0000u : 0u);
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+        const int chunk = mt * 2 + vcs;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vs + (chunk >> 3) * KvTile<D>::kBoxBytes + swz128(vtok, chunk & 7), a0, a1, a2, a3);
+        a0 &= m0;
+        a1 &= m0;
+        a2 &= m8;
+        a3 &= m8;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(ot[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
     }
 }
 

@@ -44,20 +44,26 @@ struct MapKey {
     const void* base;
     long long rows;
     int d;
-    bool operator==(const MapKey& o) const { return base == o.base && rows == o.rows && d == o.d; }
+    int kind;  // 0: 2-D half-tile boxes, 1: 4-D whole-tile boxes
+    bool operator==(const MapKey& o) const {
+        return base == o.base && rows == o.rows && d == o.d && kind == o.kind;
+    }
 };
 struct MapKeyHash {
     size_t operator()(const MapKey& k) const {
-        return std::hash<const void*>()(k.base) ^ (std::hash<long long>()(k.rows) * 31u) ^ (size_t)k.d;
+        return std::hash<const void*>()(k.base) ^ (std::hash<long long>()(k.rows) * 31u) ^ (size_t)k.d ^
+               ((size_t)k.kind << 20);
     }
 };
 
-// The pool tensor viewed as [rows = num_blocks*num_kv_heads*16, head_dim] bf16 with a
-// 64-column x 16-row box (one K or V tile half) and 128-byte swizzling.  A map depends
-// only on (address, rows, head_dim), so cached maps never go stale.
-bool pool_map(CUtensorMap* out, void* base, long long rows, int d) {
+// TMA maps over one pool tensor, 128-byte swizzled (see PoolView).  A map depends only on
+// (address, rows, head_dim, kind), so cached maps never go stale.
+//   kind 0: [rows = num_blocks*num_kv_heads*16, head_dim], box 64 x 16 (a tile half, 2 KB);
+//   kind 1: (64, 16, head_dim/64, rows/16) with strides (2*head_dim, 128, 32*head_dim) bytes,
+//           box (64, 16, head_dim/64, 1): a whole (block, head) tile landing half-major.
+bool pool_map(CUtensorMap* out, void* base, long long rows, int d, int kind) {
     static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-    const MapKey key{base, rows, d};
+    const MapKey key{base, rows, d, kind};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = cache.find(key);
@@ -69,14 +75,23 @@ bool pool_map(CUtensorMap* out, void* base, long long rows, int d) {
     auto fn = encode_fn();
     if (!fn) return false;
     CUtensorMap m;
-    const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
-    const cuuint32_t box[2] = {64, 16};
-    const cuuint32_t estr[2] = {1, 1};
-    if (fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return false;
+    CUresult r;
+    if (kind == 0) {
+        const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+        const cuuint32_t box[2] = {64, 16};
+        const cuuint32_t estr[2] = {1, 1};
+        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[4] = {64, (cuuint64_t)kBlockSize, (cuuint64_t)(d / 64), (cuuint64_t)(rows / kBlockSize)};
+        const cuuint64_t strides[3] = {(cuuint64_t)d * 2, 128, (cuuint64_t)kBlockSize * d * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)kBlockSize, (cuuint32_t)(d / 64), 1};
+        const cuuint32_t estr[4] = {1, 1, 1, 1};
+        r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return false;
     std::lock_guard<std::mutex> lk(g_mu);
     if (cache.size() > 256) cache.clear();
     cache[key] = m;
@@ -101,8 +116,10 @@ int check_pool(const pa_pool* p, PoolView* v, bool need_maps) {
     v->num_kv_heads = p->num_kv_heads;
     v->head_dim = p->head_dim;
     if (need_maps) {
-        if (!pool_map(&v->tm_k, p->k_cache, rows, p->head_dim)) return PA_ERR_CUDA;
-        if (!pool_map(&v->tm_v, p->v_cache, rows, p->head_dim)) return PA_ERR_CUDA;
+        if (!pool_map(&v->tm_k, p->k_cache, rows, p->head_dim, 0)) return PA_ERR_CUDA;
+        if (!pool_map(&v->tm_v, p->v_cache, rows, p->head_dim, 0)) return PA_ERR_CUDA;
+        if (!pool_map(&v->tile_k, p->k_cache, rows, p->head_dim, 1)) return PA_ERR_CUDA;
+        if (!pool_map(&v->tile_v, p->v_cache, rows, p->head_dim, 1)) return PA_ERR_CUDA;
     }
     return PA_OK;
 }
@@ -300,6 +317,11 @@ int pa_device_status(uint32_t* flags, int32_t clear, pa_stream_t stream) {
 int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks) {
     if (batch <= 0 || num_kv_heads <= 0 || max_blocks <= 0) return 1;
     return decode_splits_for(batch, num_kv_heads, max_blocks);
+}
+
+int pa_splitkv_num_partitions(int32_t batch, int32_t num_kv_heads, int32_t max_blocks) {
+    if (batch <= 0 || num_kv_heads <= 0 || max_blocks <= 0) return 1;
+    return splitkv_partitions_for(batch, num_kv_heads, max_blocks);
 }
 
 const char* pa_status_str(int status) {

@@ -8,8 +8,8 @@
 //
 // One CTA serves one (sequence, kv head, split): the g query heads of the group are the
 // rows of one 16-row MMA tile, so each K/V byte is read from HBM once for all of them.
-// Four consumer warps take the split's blocks round-robin, each with its own running
-// softmax; the CTA merges the four, and then
+// Three consumer warps take the split's blocks round-robin, each with its own running
+// softmax, fed by one TMA producer warp; the CTA merges the three, and then
 //   * pa_decode with one split writes bf16 O;
 //   * pa_decode with S > 1 splits runs the S CTAs of a sequence/head as one thread-block
 //     cluster and merges their partials through distributed shared memory (no
@@ -29,24 +29,30 @@ namespace cg = cooperative_groups;
 namespace pa {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+// 3 consumer warps + 1 producer warp, 6 ring slots of one 16-token block each: at <= 128
+// registers and ~50 KB of shared memory four CTAs fit on an SM, so a batch of 64
+// sequences x 8 kv heads (512 CTAs) is resident in one wave on 152 SMs.
+constexpr int kConsumerWarps = 3;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 
+// The ring depth is chosen per launch (a multiple of the consumer warp count, so each
+// warp owns the slots i with i % kConsumerWarps == warp and observes every phase of its
+// slots in order, which an mbarrier parity wait relies on): shallow when many CTAs share
+// an SM, deep when the grid is small and each CTA must keep more bytes in flight.
 template <int D>
 struct DecodeShape {
-    // each consumer warp owns the slots i with i % kConsumerWarps == warp, so it observes
-    // every phase of its slots in order (what an mbarrier parity wait relies on)
-    static constexpr int kStages = 8;
-    static_assert(kStages % kConsumerWarps == 0, "slots must divide evenly among consumer warps");
-    static constexpr int kRingBytes = kStages * KvTile<D>::kStageBytes;
+    static constexpr int kMinStages = 6;
+    static constexpr int kMaxStages = 24;
     // epilogue scratch, overlaid on the ring once it is drained
     static constexpr int kWarpPartFloats = 32 + 16 * D;  // m[16], l[16], O[16][D]
     static constexpr int kCtaPartFloats = 32 + 16 * D;
     static constexpr int kEpiBytes = (kConsumerWarps * kWarpPartFloats + kCtaPartFloats) * 4;
-    static constexpr int kDataBytes = kRingBytes > kEpiBytes ? kRingBytes : kEpiBytes;
-    static constexpr int kSmemBytes = kDataBytes + 2 * kStages * 8 + 1024;
+    __host__ __device__ static constexpr int data_bytes(int stages) {
+        return stages * KvTile<D>::kStageBytes > kEpiBytes ? stages * KvTile<D>::kStageBytes : kEpiBytes;
+    }
+    __host__ __device__ static constexpr int smem_bytes(int stages) { return data_bytes(stages) + 2 * stages * 8 + 1024; }
 };
 
 struct DecodeArgs {
@@ -58,18 +64,20 @@ struct DecodeArgs {
     float* ws_lse;
     unsigned* status;
     int max_blocks, num_heads, num_kv_heads, num_blocks, group;
+    int stages;  // ring slots, a multiple of kConsumerWarps
     float scale_log2;
 };
 
-template <int D, bool TWO_ROWS, bool SPLIT>
-__global__ void __launch_bounds__(kThreads, 3) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+template <int D, int NT, bool SPLIT>
+__global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                           const __grid_constant__ CUtensorMap tm_v,
                                                           const __grid_constant__ DecodeArgs a) {
     using Sh = DecodeShape<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::kDataBytes);
-    uint64_t* empty = full + Sh::kStages;
+    const int stages = a.stages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::data_bytes(stages));
+    uint64_t* empty = full + stages;
 
     const int split = blockIdx.x, nsplit = gridDim.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -86,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const __grid_consta
     const int n = max(0, min(per, nb - blk0));
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < Sh::kStages; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -94,69 +102,75 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const __grid_consta
     }
     __syncthreads();
 
-    constexpr int kC = Rows<TWO_ROWS>::kC;
-    float o[D / 8][kC];
+    float ot[NT][D / 16][4];
 #pragma unroll
-    for (int j = 0; j < D / 8; ++j)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < kC; ++c) o[j][c] = 0.f;
-    RowState rs;
-    rs.init();
+        for (int mt = 0; mt < D / 16; ++mt) ot[nt][mt][0] = ot[nt][mt][1] = ot[nt][mt][2] = ot[nt][mt][3] = 0.f;
+    HeadState<NT> hs;
+    hs.init();
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
         }
-        produce_kv_blocks<D, Sh::kStages>(smem, full, empty, &tm_k, &tm_v,
+        produce_kv_blocks<D>(smem, stages, full, empty, &tm_k, &tm_v,
                                           a.block_tables + (size_t)b * a.max_blocks + blk0, n, a.num_blocks,
                                           a.num_kv_heads, kvh, a.status, l2_evict_first_policy());
     } else {
-        const int r0 = lane >> 2;
-        const __nv_bfloat16* qg = a.q + ((size_t)b * a.num_heads + (size_t)kvh * g) * D;
-        uint32_t qa[D / 16][Rows<TWO_ROWS>::kA];
-        load_q_frags<D, TWO_ROWS>(qa, r0 < g ? qg + r0 * D : nullptr,
-                                  (TWO_ROWS && r0 + 8 < g) ? qg + (r0 + 8) * D : nullptr);
+        uint32_t qb[NT][D / 16][2];
+        load_q_heads<D, NT>(qb, a.q + ((size_t)b * a.num_heads + (size_t)kvh * g) * D, g);
         bool ok = true;
         for (int i = warp; i < n; i += kConsumerWarps) {
-            const int st = i % Sh::kStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / Sh::kStages) & 1));
+            const int st = i % stages;
+            ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / stages) & 1));
             if (!ok) break;
             uint8_t* kt = smem + st * KvTile<D>::kStageBytes;
             uint8_t* vt = kt + KvTile<D>::kTileBytes;
             const int valid = min(kBlockSize, L - (blk0 + i) * kBlockSize);
-            block_step<D, TWO_ROWS>(smem_u32(kt), smem_u32(vt), qa, o, rs, valid, valid, valid, a.scale_log2);
+            block_step_heads<D, NT>(smem_u32(kt), smem_u32(vt), qb, ot, hs, valid, a.scale_log2);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
         if (!ok && lane == 0) atomicOr(a.status, kDevTimeout);
-        rs.l_a += __shfl_xor_sync(0xffffffffu, rs.l_a, 1);
-        rs.l_a += __shfl_xor_sync(0xffffffffu, rs.l_a, 2);
-        rs.l_b += __shfl_xor_sync(0xffffffffu, rs.l_b, 1);
-        rs.l_b += __shfl_xor_sync(0xffffffffu, rs.l_b, 2);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float l = hs.l[nt][j];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                hs.l[nt][j] = l;
+            }
     }
     __syncthreads();  // ring drained: every issued copy has landed and been consumed
 
-    // ---- per-warp partials -> one CTA partial (unnormalised O, max m, sum l per row)
+    // ---- per-warp partials -> one CTA partial (unnormalised O, max m, sum l per head)
     float* part = reinterpret_cast<float*>(smem);
     float* cta = part + kConsumerWarps * Sh::kWarpPartFloats;  // m[16], l[16], O[16][D]
     if (warp < kConsumerWarps) {
-        const int r0 = lane >> 2, c = (lane & 3) * 2;
+        const int gid = lane >> 2, h0 = (lane & 3) * 2;
         float* pm = part + warp * Sh::kWarpPartFloats;
-        if ((lane & 3) == 0) {
-            pm[r0] = rs.m_a;
-            pm[16 + r0] = rs.l_a;
-            if (TWO_ROWS) {
-                pm[r0 + 8] = rs.m_b;
-                pm[16 + r0 + 8] = rs.l_b;
-            }
-        }
         float* po = pm + 32;
 #pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-            *reinterpret_cast<float2*>(po + r0 * D + j * 8 + c) = make_float2(o[j][0], o[j][1]);
-            if constexpr (TWO_ROWS)
-                *reinterpret_cast<float2*>(po + (r0 + 8) * D + j * 8 + c) = make_float2(o[j][2], o[j][3]);
+        for (int nt = 0; nt < NT; ++nt) {
+            const int ha = nt * 8 + h0;
+            if (gid == 0) {
+                pm[ha] = hs.m[nt][0];
+                pm[ha + 1] = hs.m[nt][1];
+                pm[16 + ha] = hs.l[nt][0];
+                pm[16 + ha + 1] = hs.l[nt][1];
+            }
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+                const int d0 = mt * 16 + gid;
+                po[ha * D + d0] = ot[nt][mt][0];
+                po[(ha + 1) * D + d0] = ot[nt][mt][1];
+                po[ha * D + d0 + 8] = ot[nt][mt][2];
+                po[(ha + 1) * D + d0 + 8] = ot[nt][mt][3];
+            }
         }
     }
     __syncthreads();
@@ -204,82 +218,139 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(const __grid_consta
         }
         return;
     }
-    // ---- cluster merge: CTA `rank` finalises a slice of the g x D outputs, reading every
-    // CTA's partial through distributed shared memory (lane r reads CTA r).
+    // ---- cluster merge: CTA `rank` finalises a slice of the g x D outputs from every CTA's
+    // partial, read through distributed shared memory in two rounds: first all (m, l) pairs
+    // (one remote load per thread), then the O slices as independent 16-byte loads.
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
+    float* wgt = part;  // [nsplit][16] merge weights, then den[16] (the warp partials are done)
+    float* den = part + 16 * 16;
     const int rank = static_cast<int>(cluster.block_rank());
-    const int slice = (E + nsplit - 1) / nsplit;
-    const int e0 = rank * slice, e1 = min(E, e0 + slice);
-    for (int e = e0 + warp; e < e1; e += kThreads / 32) {
-        const int h = e / D;
-        float mr = -INFINITY, lr = 0.f, orr = 0.f;
-        if (lane < nsplit) {
-            const float* rc = cluster.map_shared_rank(cta, lane);
-            mr = rc[h];
-            lr = rc[16 + h];
-            orr = rc[32 + e];
+    for (int t = threadIdx.x; t < nsplit * g; t += kThreads) {
+        const int r = t / g, h = t % g;
+        const float* rc = cluster.map_shared_rank(cta, r);
+        wgt[r * 16 + h] = rc[h];
+        wgt[256 + 32 + r * 16 + h] = rc[16 + h];
+    }
+    __syncthreads();
+    if (threadIdx.x < g) {
+        const int h = threadIdx.x;
+        float M = -INFINITY;
+        for (int r = 0; r < nsplit; ++r) M = fmaxf(M, wgt[r * 16 + h]);
+        float dsum = 0.f;
+        for (int r = 0; r < nsplit; ++r) {
+            const float m = wgt[r * 16 + h];
+            const float w = m == -INFINITY ? 0.f : fast_exp2(m - M);
+            wgt[r * 16 + h] = w;
+            dsum += w * wgt[256 + 32 + r * 16 + h];
         }
-        const float M = warp_max(mr);
-        const float wt = (mr != -INFINITY) ? fast_exp2(mr - M) : 0.f;
-        const float num = warp_sum(wt * orr);
-        const float den = warp_sum(wt * lr);
-        if (lane == 0) outg[e] = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
+        den[h] = dsum;
+    }
+    __syncthreads();
+    const int quads = E / 4;
+    const int qper = (quads + nsplit - 1) / nsplit;
+    for (int qd = rank * qper + threadIdx.x; qd < min(quads, (rank + 1) * qper); qd += kThreads) {
+        const int e = qd * 4, h = e / D;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int r = 0; r < nsplit; ++r) {
+            const float w = wgt[r * 16 + h];
+            const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(cta, r) + 32 + e);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+        }
+        const float inv = den[h] > 0.f ? 1.f / den[h] : 0.f;
+        *reinterpret_cast<__nv_bfloat162*>(outg + e) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        *reinterpret_cast<__nv_bfloat162*>(outg + e + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     }
     cluster.sync();  // keep this CTA's partial alive until every reader is done
 }
 
-// out[r, :] = sum_p exp(lse_p - M) O_p / sum_p exp(lse_p - M), one warp per (seq, head).
+// out[r, :] = sum_p exp(lse_p - M) O_p / sum_p exp(lse_p - M) with M = max_p lse_p.
+// One CTA of 8 warps per (sequence, head) row: every warp finds M from the row's lse values
+// (one load per lane), then warp w accumulates partitions p = w, w+8, ... with lane l
+// owning elements 4l..4l+3; the eight partial sums meet in shared memory.
+constexpr int kCombineWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ ws_o,
-                                                      const float* __restrict__ ws_lse, int rows, int P,
-                                                      __nv_bfloat16* __restrict__ out) {
-    const int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (r >= rows) return;
-    constexpr int kPer = D / 32;
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const float* __restrict__ ws_o,
+                                                                     const float* __restrict__ ws_lse, int P,
+                                                                     __nv_bfloat16* __restrict__ out) {
+    constexpr int kQuads = D / 4;
+    __shared__ float4 part[kCombineWarps][kQuads];
+    __shared__ float dpart[kCombineWarps];
+    const int r = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float* lse = ws_lse + (size_t)r * P;
-    const float* op = ws_o + (size_t)r * P * D + lane * kPer;
     float M = -INFINITY;
-    for (int p = lane; p < P; p += 32) M = fmaxf(M, lse[p]);
+    for (int p = lane; p < P; p += 32) M = fmaxf(M, __ldg(lse + p));
     M = warp_max(M);
-    float acc[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) acc[j] = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    if (M != -INFINITY) {
-        for (int p = 0; p < P; ++p) {
-            const float lp = lse[p];
-            if (lp == -INFINITY) continue;
-            const float w = fast_exp2((lp - M) * kLog2e);
+    if (M != -INFINITY && lane < kQuads) {
+        const float4* op = reinterpret_cast<const float4*>(ws_o + (size_t)r * P * D) + lane;
+#pragma unroll 4
+        for (int p = warp; p < P; p += kCombineWarps) {
+            const float lp = __ldg(lse + p);
+            const float w = lp == -INFINITY ? 0.f : fast_exp2((lp - M) * kLog2e);
+            const float4 v = __ldg(op + (size_t)p * kQuads);  // empty partitions hold zeros
             den += w;
-            if (kPer == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(op + (size_t)p * D);
-                acc[0] += w * v.x;
-                acc[1] += w * v.y;
-                acc[2] += w * v.z;
-                acc[3] += w * v.w;
-            } else {
-                const float2 v = *reinterpret_cast<const float2*>(op + (size_t)p * D);
-                acc[0] += w * v.x;
-                acc[1] += w * v.y;
-            }
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
         }
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    __nv_bfloat16* dst = out + (size_t)r * D + lane * kPer;
+    if (lane < kQuads) part[warp][lane] = acc;
+    if (lane == 0) dpart[warp] = den;
+    __syncthreads();
+    if (warp == 0 && lane < kQuads) {
+        float4 t = part[0][lane];
+        float dt = dpart[0];
 #pragma unroll
-    for (int j = 0; j < kPer; j += 2)
-        *reinterpret_cast<__nv_bfloat162*>(dst + j) = __floats2bfloat162_rn(acc[j] * inv, acc[j + 1] * inv);
+        for (int w = 1; w < kCombineWarps; ++w) {
+            t.x += part[w][lane].x;
+            t.y += part[w][lane].y;
+            t.z += part[w][lane].z;
+            t.w += part[w][lane].w;
+            dt += dpart[w];
+        }
+        const float inv = dt > 0.f ? 1.f / dt : 0.f;
+        __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(out + (size_t)r * D + lane * 4);
+        dst[0] = __floats2bfloat162_rn(t.x * inv, t.y * inv);
+        dst[1] = __floats2bfloat162_rn(t.z * inv, t.w * inv);
+    }
 }
 
-template <int D, bool TWO_ROWS, bool SPLIT>
+// Ring slots per CTA.  Measured on GB300: 6 slots of 8 KB (three per consumer warp pair of
+// K+V blocks) with four CTAs per SM beat deeper rings at every grid size tried -- a deeper
+// ring costs residency (fewer CTAs per SM) more than it gains in bytes in flight.
+template <int D>
+int stages_for(int /*ctas*/) {
+    using Sh = DecodeShape<D>;
+    // PA_DECODE_STAGES=n forces the ring depth (rounded to the warp count, clamped), for tuning
+    static const int forced = [] {
+        const char* e = std::getenv("PA_DECODE_STAGES");
+        return e ? std::atoi(e) : 0;
+    }();
+    if (forced > 0)
+        return std::max(Sh::kMinStages, std::min(Sh::kMaxStages, (forced / kConsumerWarps) * kConsumerWarps));
+    return D == 128 ? 6 : 12;
+}
+
+template <int D, int NT, bool SPLIT>
 cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cudaStream_t stream) {
     using Sh = DecodeShape<D>;
-    auto kern = decode_kernel<D, TWO_ROWS, SPLIT>;
+    auto kern = decode_kernel<D, NT, SPLIT>;
     static bool configured = false;  // per instantiation; attribute setting is idempotent
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemBytes);
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Sh::smem_bytes(Sh::kMaxStages));
+        if (e != cudaSuccess) return e;
+        // one carveout (all shared memory) for every ring depth, so launches of different
+        // depths do not reconfigure the SMs between kernels
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         if (!SPLIT) {
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -301,11 +372,12 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cuda
     da.num_blocks = pool.num_blocks;
     da.group = a.num_heads / pool.num_kv_heads;
     da.scale_log2 = a.scale * kLog2e;
+    da.stages = stages_for<D>(nsplit * pool.num_kv_heads * a.batch);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nsplit, pool.num_kv_heads, a.batch);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = Sh::kSmemBytes;
+    cfg.dynamicSmemBytes = Sh::smem_bytes(da.stages);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (!SPLIT && nsplit > 1) {
@@ -316,17 +388,17 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cuda
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, kern, pool.tm_k, pool.tm_v, da);
+    return cudaLaunchKernelEx(&cfg, kern, pool.tile_k, pool.tile_v, da);
 }
 
 template <bool SPLIT>
 cudaError_t dispatch(const PoolView& pool, const AttnArgs& a, int nsplit, cudaStream_t stream) {
     const int g = a.num_heads / pool.num_kv_heads;
     if (pool.head_dim == 128)
-        return g > 8 ? launch_one<128, true, SPLIT>(pool, a, nsplit, stream)
-                     : launch_one<128, false, SPLIT>(pool, a, nsplit, stream);
-    return g > 8 ? launch_one<64, true, SPLIT>(pool, a, nsplit, stream)
-                 : launch_one<64, false, SPLIT>(pool, a, nsplit, stream);
+        return g > 8 ? launch_one<128, 2, SPLIT>(pool, a, nsplit, stream)
+                     : launch_one<128, 1, SPLIT>(pool, a, nsplit, stream);
+    return g > 8 ? launch_one<64, 2, SPLIT>(pool, a, nsplit, stream)
+                 : launch_one<64, 1, SPLIT>(pool, a, nsplit, stream);
 }
 
 int max_cluster_splits() {
@@ -334,14 +406,14 @@ int max_cluster_splits() {
     static int cached = 0;
     if (cached) return cached;
     int best = 8;
-    auto kern = decode_kernel<128, false, false>;
+    auto kern = decode_kernel<128, 1, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DecodeShape<128>::kSmemBytes) ==
-            cudaSuccess) {
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             DecodeShape<128>::smem_bytes(DecodeShape<128>::kMaxStages)) == cudaSuccess) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(16, 1, 1);
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = DecodeShape<128>::kSmemBytes;
+        cfg.dynamicSmemBytes = DecodeShape<128>::smem_bytes(DecodeShape<128>::kMinStages);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 16;
@@ -369,10 +441,19 @@ int decode_splits_for(int batch, int num_kv_heads, int max_blocks) {
     const int items = batch * num_kv_heads;
     const int sms = device_info().num_sms;
     if (items >= sms) return 1;
-    int s = (2 * sms + items - 1) / items;  // aim for about two CTAs per SM
+    int s = std::max(1, (4 * sms) / items);  // fill one wave of four CTAs per SM
     s = std::min(s, max_cluster_splits());
     s = std::min(s, std::max(1, max_blocks / 4));  // at least ~4 blocks per split
     return std::max(1, s);
+}
+
+int splitkv_partitions_for(int batch, int num_kv_heads, int max_blocks) {
+    // a power of two that fills one wave of four CTAs per SM, keeping >= 8 blocks per partition
+    const int items = std::max(1, batch * num_kv_heads);
+    const int want = std::max(1, (4 * device_info().num_sms) / items);
+    int p = 1;
+    while (p * 2 <= want && p * 2 <= 64 && (max_blocks / (p * 2)) >= 8) p *= 2;
+    return p;
 }
 
 cudaError_t launch_decode(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
@@ -387,12 +468,11 @@ cudaError_t launch_decode_splitkv(const PoolView& pool, const AttnArgs& a, cudaS
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, int batch, int num_heads, int head_dim,
                            int num_partitions, void* out, cudaStream_t stream) {
     const int rows = batch * num_heads;
-    const int blocks = (rows * 32 + 255) / 256;
     auto* o = static_cast<__nv_bfloat16*>(out);
     if (head_dim == 128)
-        combine_kernel<128><<<blocks, 256, 0, stream>>>(ws_o, ws_lse, rows, num_partitions, o);
+        combine_kernel<128><<<rows, kCombineWarps * 32, 0, stream>>>(ws_o, ws_lse, num_partitions, o);
     else
-        combine_kernel<64><<<blocks, 256, 0, stream>>>(ws_o, ws_lse, rows, num_partitions, o);
+        combine_kernel<64><<<rows, kCombineWarps * 32, 0, stream>>>(ws_o, ws_lse, num_partitions, o);
     return cudaGetLastError();
 }
 

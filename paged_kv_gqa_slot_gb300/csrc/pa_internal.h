@@ -8,9 +8,13 @@
 
 namespace pa {
 
-// A validated pool: [num_blocks, num_kv_heads, 16, head_dim] bf16 for K and for V,
-// plus one 2-D TMA map per tensor that views it as [num_blocks*num_kv_heads*16 rows,
-// head_dim] with a 64-element x 16-row box and 128-byte swizzling.
+// A validated pool: [num_blocks, num_kv_heads, 16, head_dim] bf16 for K and for V, with
+// two TMA maps per tensor, both with 128-byte swizzling:
+//   tm_k / tm_v   2-D [rows = num_blocks*num_kv_heads*16, head_dim], box 64 columns x 16 rows
+//                 (one 64-column half of a (block, head) tile, 2 KB);
+//   tile_k/tile_v 4-D (64 columns, 16 rows, head_dim/64 halves, num_blocks*num_kv_heads tiles)
+//                 with the halves dimension strided 128 B and the rows 2*head_dim B, box =
+//                 one whole (block, head) tile, which lands as [half][16 rows][128 B].
 struct PoolView {
     void* k;
     void* v;
@@ -19,6 +23,8 @@ struct PoolView {
     int head_dim;
     CUtensorMap tm_k;
     CUtensorMap tm_v;
+    CUtensorMap tile_k;
+    CUtensorMap tile_v;
 };
 
 struct DeviceInfo {
@@ -55,8 +61,13 @@ cudaError_t launch_decode_splitkv(const PoolView& pool, const AttnArgs& a, cudaS
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, int batch, int num_heads, int head_dim,
                            int num_partitions, void* out, cudaStream_t stream);
 cudaError_t launch_prefill(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
+// tcgen05 chunked prefill: head_dim 128 and a group size dividing 128
+bool prefill_tc_supported(int head_dim, int group);
+cudaError_t launch_prefill_tc(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
 
 // Split count the decode launcher picks for a problem (exposed for tests and tuning).
 int decode_splits_for(int batch, int num_kv_heads, int max_blocks);
+// Partition count suggested for pa_decode_splitkv.
+int splitkv_partitions_for(int batch, int num_kv_heads, int max_blocks);
 
 }  // namespace pa

@@ -1,4 +1,6 @@
-// pa_prefill.cu -- chunked prefill over a cached paged prefix (warp-MMA kernel).
+// pa_prefill.cu -- chunked prefill over a cached paged prefix (warp-MMA kernel, used for the
+// shapes the tcgen05 kernel in pa_prefill_tc.cu does not take: head_dim 64, or a group size
+// that does not divide 128).
 //
 // Method: "Qwen3-4B / 8B / 32B", sections "Warm Prefix-Cache TTFT" (most of a prompt
 // is a warm prefix-cache hit; only the new chunk is computed) and "Architecture Notes"
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const __grid_cons
             prefetch_tensormap(&tm_v);
         }
         // the prefix blocks are shared by every sequence of a prefix-cache hit: keep them in L2
-        produce_kv_blocks<D, Sh::kStages>(smem, full, empty, &tm_k, &tm_v, a.block_tables + (size_t)b * a.max_blocks,
+        produce_kv_blocks<D>(smem, Sh::kStages, full, empty, &tm_k, &tm_v, a.block_tables + (size_t)b * a.max_blocks,
                                           nb, a.num_blocks, a.num_kv_heads, kvh, a.status, l2_evict_last_policy());
         return;
     }
@@ -170,13 +172,14 @@ cudaError_t launch_mma(const PoolView& pool, const AttnArgs& a, cudaStream_t str
     const long long rows = (long long)a.max_chunk * pa_.group;
     const int tiles = static_cast<int>((rows + kRows - 1) / kRows);
     dim3 grid(std::max(1, tiles), pool.num_kv_heads, a.batch);
-    kern<<<grid, kThreads, Sh::kSmemBytes, stream>>>(pool.tm_k, pool.tm_v, pa_);
+    kern<<<grid, kThreads, Sh::kSmemBytes, stream>>>(pool.tile_k, pool.tile_v, pa_);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
+    if (prefill_tc_supported(pool.head_dim, a.num_heads / pool.num_kv_heads)) return launch_prefill_tc(pool, a, stream);
     if (pool.head_dim == 128) return launch_mma<128>(pool, a, stream);
     return launch_mma<64>(pool, a, stream);
 }
