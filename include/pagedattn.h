@@ -53,7 +53,8 @@ enum pa_status {
     PA_ERR_UNSUPPORTED = -2,  /* block size, head dim or group size outside the compiled set */
     PA_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
     PA_ERR_OUT_OF_RANGE = -4, /* pa_device_status: a block id / slot / length outside the pool was skipped */
-    PA_ERR_TIMEOUT = -5       /* pa_device_status: a pipeline wait ran out (a bug, never expected) */
+    PA_ERR_TIMEOUT = -5,      /* pa_device_status: a pipeline wait ran out (a bug, never expected) */
+    PA_ERR_TOO_LARGE = -6     /* pa_decode_splitkv_noalloc: the request does not fit its static scratch */
 };
 
 /* Device status bits reported by pa_device_status. */
@@ -155,6 +156,31 @@ int pa_prefill_chunked(const pa_pool *pool, const void *q, const int32_t *cu_q_l
  * first), PA_ERR_INVALID_ARG for a NULL flags pointer, PA_ERR_CUDA on a CUDA error.
  */
 int pa_device_status(uint32_t *flags, int32_t clear, pa_stream_t stream);
+
+/*
+ * pa_decode_splitkv_noalloc -- split-KV decode and its log-sum-exp merge in one call that
+ * allocates nothing and takes no workspace: out = pa_combine(pa_decode_splitkv(...)).
+ * The pages have no counterpart of this call; it exists for callers that cannot allocate
+ * device memory -- an engine whose memory is a fixed arena owned by someone else, a plugin
+ * in a host framework that exposes no allocator, or a serving loop that must never call
+ * cudaMalloc on its hot path (an allocation there can synchronise the whole device).
+ *   Arguments as pa_decode_splitkv plus out [batch, num_heads, head_dim] bf16.
+ *   The partition results live in one static device array of pa_noalloc_scratch_bytes()
+ *   bytes (8 MiB) inside the library, held by every GPU that loads the library until the
+ *   process exits.  A request whose workspace (pa_splitkv_workspace_bytes) exceeds it
+ *   returns PA_ERR_TOO_LARGE before any launch.
+ *   The first call on a device looks up the array's device address (one-time set-up on that
+ *   device); make that first call before capturing any stream into a CUDA graph.
+ *   Every call uses the same array, so calls that may run at the same time on the GPU
+ *   (different streams, or different host threads) race and must be serialised by the
+ *   caller.  Nothing needs clearing between calls: each call overwrites every slot it reads.
+ */
+int pa_decode_splitkv_noalloc(const pa_pool *pool, const void *q, const int32_t *block_tables, int32_t max_blocks,
+                              const int32_t *seq_lens, int32_t batch, int32_t num_heads, float scale,
+                              int32_t num_partitions, void *out, pa_stream_t stream);
+
+/* Size in bytes of the static scratch array of pa_decode_splitkv_noalloc. */
+size_t pa_noalloc_scratch_bytes(void);
 
 /* Number of cluster splits pa_decode uses for this shape on the current device. */
 int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);

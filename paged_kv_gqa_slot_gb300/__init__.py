@@ -22,7 +22,7 @@ import torch
 
 __all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_decode_splitkv", "pa_combine", "pa_prefill_chunked",
            "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "pa_splitkv_num_partitions",
-           "PagedAttnError",
+           "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes", "PagedAttnError",
            "library", "library_path", "BLOCK_SIZE", "EXPORTED_SYMBOLS"]
 
 BLOCK_SIZE = 16
@@ -30,7 +30,7 @@ PKG = Path(__file__).resolve().parent
 _LIB_PATH = PKG / "libpagedattn.so"
 EXPORTED_SYMBOLS = ("pa_kv_append", "pa_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv", "pa_combine",
                     "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_splitkv_num_partitions",
-                    "pa_status_str", "pa_version")
+                    "pa_status_str", "pa_version", "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes")
 
 PA_OK = 0
 PA_ERR_INVALID_ARG = -1
@@ -38,6 +38,7 @@ PA_ERR_UNSUPPORTED = -2
 PA_ERR_CUDA = -3
 PA_ERR_OUT_OF_RANGE = -4
 PA_ERR_TIMEOUT = -5
+PA_ERR_TOO_LARGE = -6
 PA_DEV_OUT_OF_RANGE = 1
 PA_DEV_TIMEOUT = 2
 
@@ -81,6 +82,8 @@ def library() -> ctypes.CDLL:
         "pa_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32, P]),
         "pa_decode_num_splits": (ctypes.c_int, [I32, I32, I32]),
         "pa_splitkv_num_partitions": (ctypes.c_int, [I32, I32, I32]),
+        "pa_decode_splitkv_noalloc": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, I32, P, P]),
+        "pa_noalloc_scratch_bytes": (SZ, []),
         "pa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "pa_version": (ctypes.c_int, []),
     }
@@ -179,6 +182,26 @@ def pa_decode_splitkv(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor,
                                      _stream(stream))
     _check(rc, "pa_decode_splitkv")
     return ws_o, ws_lse
+
+
+def pa_decode_splitkv_noalloc(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                              scale: float, num_partitions: int, out: Optional[torch.Tensor] = None,
+                              stream=None) -> torch.Tensor:
+    """Split-KV decode + merge with no workspace argument: for callers that cannot allocate
+    device memory (see include/pagedattn.h).  Pass a preallocated `out` to allocate nothing
+    at all; its partition results live in a static array inside the library."""
+    B, Hq, _ = q.shape
+    out = torch.empty_like(q) if out is None else out
+    rc = library().pa_decode_splitkv_noalloc(pool.ref, _dev(q, torch.bfloat16, "q"),
+                                             _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                             _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale),
+                                             int(num_partitions), _dev(out, torch.bfloat16, "out"), _stream(stream))
+    _check(rc, "pa_decode_splitkv_noalloc")
+    return out
+
+
+def pa_noalloc_scratch_bytes() -> int:
+    return int(library().pa_noalloc_scratch_bytes())
 
 
 def pa_combine(ws_o: torch.Tensor, ws_lse: torch.Tensor, out: Optional[torch.Tensor] = None,

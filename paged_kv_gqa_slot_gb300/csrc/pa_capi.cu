@@ -332,6 +332,7 @@ const char* pa_status_str(int status) {
         case PA_ERR_CUDA: return "PA_ERR_CUDA";
         case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
         case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+        case PA_ERR_TOO_LARGE: return "PA_ERR_TOO_LARGE";
         default: return "PA_ERR_UNKNOWN";
     }
 }

@@ -96,5 +96,12 @@ def test_validation_rejects_before_launch(lib):
     assert lib.pa_kv_append(P(ok_pool), FAKE, FAKE, None, 3, None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_kv_append(P(ok_pool), FAKE, FAKE, FAKE, -1, None) == pa.PA_ERR_INVALID_ARG
     assert lib.pa_kv_append(P(ok_pool), FAKE, FAKE, FAKE, 0, None) == pa.PA_OK
+    # the workspace-free split-KV call refuses what does not fit its static scratch, before any launch
+    assert lib.pa_noalloc_scratch_bytes() == 8 << 20
+    assert lib.pa_decode_splitkv_noalloc(P(ok_pool), FAKE, FAKE, 4, FAKE, 1, 64, 0.1, 4096, FAKE, None) == \
+        pa.PA_ERR_TOO_LARGE
+    assert lib.pa_decode_splitkv_noalloc(P(_pool(d=96)), FAKE, FAKE, 4, FAKE, 1, 4, 0.1, 8, FAKE, None) == \
+        pa.PA_ERR_UNSUPPORTED
+    assert lib.pa_decode_splitkv_noalloc(P(ok_pool), FAKE, FAKE, 4, FAKE, 0, 4, 0.1, 8, FAKE, None) == pa.PA_OK
     # status needs a flags pointer
     assert lib.pa_device_status(None, 1, None) == pa.PA_ERR_INVALID_ARG
