@@ -90,6 +90,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// 2-D tiled load multicast to the CTAs of `mask` in this cluster: the box lands at the same
+// shared-memory offset in each of them and completes on their mbarriers at `bar`'s offset.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                               uint16_t mask, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
+        : "memory");
+}
+
 // 4-D tiled load: one whole (block, head) tile of a pool through its 4-D map.
 __device__ __forceinline__ void tma_load_tile(void* dst, const CUtensorMap* map, int tile, uint64_t* bar,
                                               uint64_t policy) {
@@ -210,6 +221,15 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// As tc_commit, arriving on the mbarrier at `bar`'s offset in every CTA of `mask`.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
 }
 
 // 32 consecutive TMEM columns of this thread's lane (warp w reads lanes 32*(w%4)..+31),

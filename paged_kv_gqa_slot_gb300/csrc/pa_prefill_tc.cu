@@ -22,6 +22,13 @@
 // Warp roles: 0-3 softmax (TMEM lanes 32w..32w+31), 4 MMA issue + TMEM owner, 5 TMA.
 // 96 KB of shared memory and 256 TMEM columns per CTA: two CTAs share an SM, so one's
 // softmax overlaps the other's MMAs.
+// The c CTAs that hold consecutive query tiles of one (sequence, kv head) form a
+// thread-block cluster and read the same K/V: each issues 1/c of every stage's TMA boxes
+// with multicast to all members, and every member's MMA thread releases a stage to all of
+// them (multicast commit), so a stage refills once the whole cluster is done with it.  A
+// TMA stream of small (2 KB) boxes is limited by boxes per second per SM, not bytes, so
+// this divides the limiting cost by c.  Members walk the union of their key tiles (a tile
+// some other member needs is received and released without compute).
 #include <algorithm>
 #include <cstdlib>
 
@@ -65,6 +72,13 @@ struct TcArgs {
     float scale_log2;
 };
 
+// Key tiles a query tile needs: keys [0, kmax) with kmax the last query's position + 1.
+__device__ __forceinline__ int tile_key_count(int mt, int tpt, int C, int L) {
+    const int tok0 = mt * tpt;
+    if (mt < 0 || tok0 >= C) return 0;
+    return L - C + tok0 + min(tpt, C - tok0);
+}
+
 __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
                                                                  const __grid_constant__ TcArgs a) {
@@ -72,33 +86,39 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t crank, cnum;
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
+    asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(cnum));
+    const int rank = static_cast<int>(crank), csize = static_cast<int>(cnum);
+    const uint16_t all_mask = static_cast<uint16_t>((1u << csize) - 1u);
     const int mt = gridDim.x - 1 - blockIdx.x;  // the latest (longest) query tiles first
     const int kvh = blockIdx.y, b = blockIdx.z;
     const int g = a.group, tpt = kRows / g;
     const int q0 = a.cu_q_lens[b];
     const int C = a.cu_q_lens[b + 1] - q0;
     const int L = a.seq_lens[b];
-    if (C < 0 || L < C || L > a.max_blocks * kBlockSize) {
-        if (threadIdx.x == 0 && mt == 0 && kvh == 0) atomicOr(a.status, kDevOutOfRange);
+    if (C < 0 || L < C || L > a.max_blocks * kBlockSize) {  // the same for the whole cluster
+        if (threadIdx.x == 0 && mt == gridDim.x - 1 && kvh == 0) atomicOr(a.status, kDevOutOfRange);
         return;
     }
     const int tok0 = mt * tpt;
-    if (tok0 >= C) return;  // this sequence's chunk is shorter than the grid allows
-    const int ntok = min(tpt, C - tok0);
+    const int ntok = tok0 < C ? min(tpt, C - tok0) : 0;
     const int rows_valid = ntok * g;
     const int pos0 = L - C + tok0;                          // position of the tile's first query
-    const int kmax = pos0 + ntok;                           // keys [0, kmax) are visible to some row
-    const int ntiles = (kmax + kKeys - 1) / kKeys;
-    const int nblk = (kmax + kBlockSize - 1) / kBlockSize;  // pool blocks read
+    const int ntiles = (tile_key_count(mt, tpt, C, L) + kKeys - 1) / kKeys;  // this CTA's tiles
+    int kmax_cl = 0;                                        // keys any member of the cluster needs
+    for (int r = 0; r < csize; ++r) kmax_cl = max(kmax_cl, tile_key_count(mt + rank - r, tpt, C, L));
+    const int ntiles_cl = (kmax_cl + kKeys - 1) / kKeys;
+    const int nblk = (kmax_cl + kBlockSize - 1) / kBlockSize;  // pool blocks read
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
-            mbar_init(&bars->k_empty[s], 1);
+            mbar_init(&bars->k_empty[s], csize);  // one release from every member
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars->v_full[s], 1);
-            mbar_init(&bars->v_empty[s], 1);
+            mbar_init(&bars->v_empty[s], csize);
         }
         mbar_init(&bars->q_full, 128);
         mbar_init(&bars->s_full, 1);
@@ -114,12 +134,16 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
     }
     tc_fence_before();
     __syncthreads();
+    // every member's barriers exist before any multicast box or release can reach them
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 5) {
         // ------------------------------------------------------------ TMA producer
-        // issue order K(0), K(1), V(0), K(2), V(1), ...: K runs one tile ahead of V
+        // issue order K(0), K(1), V(0), K(2), V(1), ...: K runs one tile ahead of V.  Of the
+        // 8 boxes of a stage (4 blocks x 2 column halves) this member issues those with
+        // index % csize == rank, multicast to the whole cluster.
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
@@ -127,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
         const uint64_t pol = l2_evict_last_policy();  // prefix blocks are shared across sequences
         const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks;
         const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;  // past the pool: zero fill
-        // pool rows of the four blocks of tile j, from a warp-held window of 32 table entries
         int c0 = 0;
         int cur = lane < nblk ? __ldg(bt + lane) : 0;
         int nxt = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
@@ -148,12 +171,12 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
                 rows[t] = lb < nblk ? (id * a.num_kv_heads + kvh) * kBlockSize : oob_row;
             }
         };
+        const bool my_box = lane < 8 && (lane % csize) == rank;
         bool ok = true;
         int k_issued = 0, v_issued = 0;
         int rows_k[4], rows_v[4];
-        for (int step = 0; step <= ntiles && ok; ++step) {
-            // K(step) then V(step - 1)
-            if (step < ntiles) {
+        for (int step = 0; step <= ntiles_cl && ok; ++step) {
+            if (step < ntiles_cl) {
                 tile_rows(step, rows_k);
                 const int s = step % kKStages;
                 if (lane == 0) {
@@ -162,12 +185,11 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
                 if (ok) {
-                    // the tile's eight boxes go out from lanes 0..7 in one instruction
-                    if (lane < 8) {
+                    if (my_box) {
                         const int t = lane >> 1, h = lane & 1;
                         const int row = t == 0 ? rows_k[0] : t == 1 ? rows_k[1] : t == 2 ? rows_k[2] : rows_k[3];
-                        tma_load_2d(smem + kOffK + s * kTileBytes + h * kHalf + t * 2048, &tm_k, h * 64, row,
-                                    &bars->k_full[s], pol);
+                        tma_load_2d_mc(smem + kOffK + s * kTileBytes + h * kHalf + t * 2048, &tm_k, h * 64, row,
+                                       &bars->k_full[s], all_mask, pol);
                     }
                     ++k_issued;
                 }
@@ -180,11 +202,11 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
                 if (ok) {
-                    if (lane < 8) {
+                    if (my_box) {
                         const int t = lane >> 1, h = lane & 1;
                         const int row = t == 0 ? rows_v[0] : t == 1 ? rows_v[1] : t == 2 ? rows_v[2] : rows_v[3];
-                        tma_load_2d(smem + kOffV + s * kTileBytes + h * kHalf + t * 2048, &tm_v, h * 64, row,
-                                    &bars->v_full[s], pol);
+                        tma_load_2d_mc(smem + kOffV + s * kTileBytes + h * kHalf + t * 2048, &tm_v, h * 64, row,
+                                       &bars->v_full[s], all_mask, pol);
                     }
                     ++v_issued;
                 }
@@ -193,11 +215,17 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
             for (int t = 0; t < 4; ++t) rows_v[t] = rows_k[t];
         }
         if (lane == 0) {
-            // every copy issued must have landed before the CTA may leave
-            for (int j = max(0, k_issued - kKStages); j < k_issued; ++j)
+            // Before the CTA may leave: every stage armed here has been filled (by every
+            // member's boxes), and every member has released it (so no release can still be
+            // on its way to this CTA's barriers).
+            for (int j = max(0, k_issued - kKStages); j < k_issued; ++j) {
                 if (!mbar_wait(&bars->k_full[j % kKStages], (j / kKStages) & 1)) ok = false;
-            for (int j = max(0, v_issued - kVStages); j < v_issued; ++j)
+                if (!mbar_wait(&bars->k_empty[j % kKStages], (j / kKStages) & 1)) ok = false;
+            }
+            for (int j = max(0, v_issued - kVStages); j < v_issued; ++j) {
                 if (!mbar_wait(&bars->v_full[j % kVStages], (j / kVStages) & 1)) ok = false;
+                if (!mbar_wait(&bars->v_empty[j % kVStages], (j / kVStages) & 1)) ok = false;
+            }
             if (!ok) atomicOr(a.status, kDevTimeout);
         }
     } else if (warp == 4) {
@@ -207,37 +235,43 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
             constexpr uint32_t idesc_o = tc_idesc_bf16(kRows, kD, true);
             const uint32_t p_s = smem_u32(smem + kOffP);
             bool ok = mbar_wait(&bars->q_full, 0);
-            for (int j = 0; j <= ntiles && ok; ++j) {
-                if (j < ntiles) {
+            for (int j = 0; j <= ntiles_cl && ok; ++j) {
+                if (j < ntiles_cl) {
                     const int s = j % kKStages;
                     ok = mbar_wait(&bars->k_full[s], (j / kKStages) & 1);
-                    if (ok && j > 0) ok = mbar_wait(&bars->s_free, (j - 1) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t k_s = smem_u32(smem + kOffK + s * kTileBytes);
+                    if (ok && j < ntiles) {
+                        if (j > 0) ok = mbar_wait(&bars->s_free, (j - 1) & 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t k_s = smem_u32(smem + kOffK + s * kTileBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint64_t bd = smem_desc_sw128(k_s + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024);
-                        tc_mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint64_t bd = smem_desc_sw128(k_s + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024);
+                            tc_mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
+                        }
+                        tc_commit(&bars->s_full);
                     }
-                    tc_commit(&bars->s_full);
-                    tc_commit(&bars->k_empty[s]);
+                    if (!ok) break;
+                    tc_commit_mc(&bars->k_empty[s], all_mask);  // release the K slot cluster-wide
                 }
                 if (j > 0) {
                     const int jp = j - 1, s = jp % kVStages;
-                    ok = mbar_wait(&bars->p_full, jp & 1);
-                    if (ok) ok = mbar_wait(&bars->v_full[s], (jp / kVStages) & 1);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t v_s = smem_u32(smem + kOffV + s * kTileBytes);
+                    ok = mbar_wait(&bars->v_full[s], (jp / kVStages) & 1);
+                    if (ok && jp < ntiles) {
+                        ok = mbar_wait(&bars->p_full, jp & 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t v_s = smem_u32(smem + kOffV + s * kTileBytes);
 #pragma unroll
-                    for (int ks = 0; ks < kKeys / 16; ++ks) {
-                        const uint64_t ad = smem_desc_sw128(p_s + ks * 32, 0, 1024);
-                        const uint64_t bd = smem_desc_sw128(v_s + ks * 16 * 128, kHalf, 1024);
-                        tc_mma(tmem + kTmemO, ad, bd, idesc_o, (jp > 0 || ks > 0) ? 1u : 0u);
+                        for (int ks = 0; ks < kKeys / 16; ++ks) {
+                            const uint64_t ad = smem_desc_sw128(p_s + ks * 32, 0, 1024);
+                            const uint64_t bd = smem_desc_sw128(v_s + ks * 16 * 128, kHalf, 1024);
+                            tc_mma(tmem + kTmemO, ad, bd, idesc_o, (jp > 0 || ks > 0) ? 1u : 0u);
+                        }
+                        tc_commit(&bars->o_done);
                     }
-                    tc_commit(&bars->o_done);
-                    tc_commit(&bars->v_empty[s]);
+                    if (!ok) break;
+                    tc_commit_mc(&bars->v_empty[s], all_mask);
                 }
             }
             // every MMA issued above has finished before the tensor memory is released
@@ -344,7 +378,9 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
             if (k0 + kKeys > L) {
                 // keys at or past the sequence end: zero their V rows, whatever the slots hold.
                 // V(j) has landed: PV(j-2), the previous user of this slot, finished before
-                // PV(j-1), so only this phase of the slot's barrier can be pending.
+                // PV(j-1), so only this phase of the slot's barrier can be pending.  (The other
+                // members need these rows zeroed too and zero them themselves: every member
+                // that computes tile j reaches this point before releasing the slot.)
                 const int s = j % kVStages;
                 if (!mbar_wait(&bars->v_full[s], (j / kVStages) & 1)) {
                     ok = false;
@@ -363,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
             mbar_arrive(&bars->p_full);
         }
         if (ok && ntiles > 0) ok = mbar_wait(&bars->o_done, (ntiles - 1) & 1);
-        if (ok) {
+        if (ok && ntiles > 0) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16* dst = a.out + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD;
@@ -392,6 +428,8 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    // no member leaves while another may still multicast into its memory or release to it
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 }  // namespace
@@ -426,10 +464,29 @@ cudaError_t launch_prefill_tc(const PoolView& pool, const AttnArgs& a, cudaStrea
     t.group = a.num_heads / pool.num_kv_heads;
     t.scale_log2 = a.scale * kLog2e;
     const int tpt = kRows / t.group;
-    const int tiles = (a.max_chunk + tpt - 1) / tpt;
-    dim3 grid(std::max(1, tiles), pool.num_kv_heads, a.batch);
-    prefill_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(pool.tm_k, pool.tm_v, t);
-    return cudaGetLastError();
+    const int tiles = std::max(1, (a.max_chunk + tpt - 1) / tpt);
+    // cluster over consecutive query tiles of one (sequence, kv head): up to 4 members
+    static const int forced = [] {
+        const char* e = std::getenv("PA_PREFILL_CLUSTER");
+        return e ? std::atoi(e) : 0;
+    }();
+    int cs = forced > 0 ? forced : 4;
+    cs = std::max(1, std::min(cs, 8));
+    while (cs > 1 && cs > tiles) cs >>= 1;
+    const int gx = (tiles + cs - 1) / cs * cs;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(gx, pool.num_kv_heads, a.batch);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cs;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, pool.tm_k, pool.tm_v, t);
 }
 
 }  // namespace pa
