@@ -48,7 +48,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 KERNEL_SOURCES = {
     "decode": ["pa_decode.cu", "pa_block_attn.cuh", "pa_device.cuh"],
     "splitkv": ["pa_decode.cu", "pa_block_attn.cuh", "pa_device.cuh"],
-    "prefill": ["pa_prefill.cu", "pa_block_attn.cuh", "pa_device.cuh"],
+    "prefill": ["pa_prefill.cu", "pa_prefill_tc.cu", "pa_block_attn.cuh", "pa_device.cuh"],
     "append": ["pa_append.cu", "pa_device.cuh"],
     "combine": ["pa_decode.cu", "pa_device.cuh"],
 }

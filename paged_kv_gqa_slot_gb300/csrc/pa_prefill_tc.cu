@@ -6,30 +6,36 @@
 // over a paged KV cache).  Chunk query i of sequence s sits at position L_s - C_s + i and
 // attends causally to keys 0 .. L_s - C_s + i through the block table.
 //
-// One CTA per (128-row tile, kv head, sequence).  Rows are (query, head-of-the-group)
-// pairs, row r = query r / g, head r % g, so one K/V tile serves all g heads.  Per stage of
-// 64 keys (four 16-token pool blocks, loaded by TMA with 128-byte swizzling):
+// Rows of a query tile are (query, head-of-the-group) pairs: row r = query r / g, head r % g,
+// so one K/V tile serves all g heads; a tile holds 128 rows (128 / g queries).  One CTA per
+// SM holds TWO query tiles of the same (sequence, kv head), the i-th longest with the i-th
+// shortest (tiles T-1-i and i), so every CTA has about the same causal work.  Per stage of
+// 64 keys (four 16-token pool blocks, loaded by TMA with 128-byte swizzling), for each tile:
 //   S[128 x 64]  = Q K^T      tcgen05.mma, M=128 N=64, Q (A) from TMEM, K (B) from smem
 //   softmax      one thread per row reads its S row from TMEM, masks causally (only in
 //                tiles that cross the diagonal), keeps an online max / sum in base 2 and
 //                writes P (bf16, 128-byte swizzled) to shared memory
 //   O[128 x 128] += P V       tcgen05.mma, M=128 N=128, P (A) and V (B) from smem
-// TMEM columns: S [0,64), Q [64,128) (bf16 pairs), O [128,256).  The running max is
-// re-based lazily: O is rescaled in TMEM only when a row's max grows by more than 2^8,
-// which keeps every P <= 256 and makes rescales rare.
-// K and V have separate rings (3 and 2 slots): a K slot is handed back as soon as its
-// Q K^T has run, so the next K tiles load while the softmax and P V of this one proceed.
-// Warp roles: 0-3 softmax (TMEM lanes 32w..32w+31), 4 MMA issue + TMEM owner, 5 TMA.
-// 96 KB of shared memory and 256 TMEM columns per CTA: two CTAs share an SM, so one's
-// softmax overlaps the other's MMAs.
-// The c CTAs that hold consecutive query tiles of one (sequence, kv head) form a
+// Each tile owns 256 TMEM columns: S [0,64), Q [64,128) (bf16 pairs), O [128,256).  The
+// running max is re-based lazily: O is rescaled in TMEM only when a row's max grows by more
+// than 2^8, which keeps every P <= 256 and makes rescales rare.
+// Warp roles: 0-3 softmax of tile 0, 4-7 softmax of tile 1 (TMEM lanes 32(w%4)..+31),
+// 8 MMA issue + TMEM owner, 9 TMA loads of K, 10 TMA loads of V.  While one tile's softmax
+// runs, the other tile's MMAs do, so the tensor pipe and the special-function units
+// overlap.  A warp issues only a few TMA boxes per microsecond, so K and V have a warp each
+// and never wait on each other's ring.
+// K and V have separate 4-slot rings: a K slot is handed back as soon as both tiles' Q K^T
+// have run; 4 slots cover the L2 round trip of the next tiles.  P is double-buffered per
+// tile, so the softmax of key tile j+1 waits for P V of tile j-1 only (long finished),
+// unless O must be rescaled.
+// The c CTAs that hold consecutive tile pairs of one (sequence, kv head) form a
 // thread-block cluster and read the same K/V: each issues 1/c of every stage's TMA boxes
 // with multicast to all members, and every member's MMA thread releases a stage to all of
-// them (multicast commit), so a stage refills once the whole cluster is done with it.  A
-// TMA stream of small (2 KB) boxes is limited by boxes per second per SM, not bytes, so
-// this divides the limiting cost by c.  Members walk the union of their key tiles (a tile
-// some other member needs is received and released without compute).
+// them (multicast commit), so a stage refills once the whole cluster is done with it.
+// Members walk the union of their key tiles (a tile some other member needs is received
+// and released without compute).
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 
 #include "pa_device.cuh"
@@ -39,27 +45,36 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kRows = 128;                      // MMA M
+constexpr int kRows = 128;                      // MMA M: rows of one query tile
+constexpr int kTiles = 2;                       // query tiles per CTA
 constexpr int kKeys = 64;                       // keys per stage (MMA N of S)
-constexpr int kKStages = 3, kVStages = 2;
-constexpr int kThreads = 192;
-constexpr int kTmemCols = 256;
+constexpr int kKStages = 4, kVStages = 4, kPBufs = 2;
+constexpr int kSoftmaxThreads = kTiles * 128;
+constexpr int kMmaWarp = kSoftmaxThreads / 32, kKLoadWarp = kMmaWarp + 1, kVLoadWarp = kMmaWarp + 2;
+constexpr int kThreads = kSoftmaxThreads + 96;
+constexpr int kTmemCols = 512;
+constexpr uint32_t kTmemTile = 256;             // columns owned by one tile
 constexpr uint32_t kTmemS = 0, kTmemQ = 64, kTmemO = 128;
 constexpr int kHalf = kKeys * 128;              // [64 keys][64 columns] bf16 = 8 KB
-constexpr int kTileBytes = 2 * kHalf;           // one K or V tile (two column halves), 16 KB
+constexpr int kTileBytes = 2 * kHalf;           // one K or V stage (two column halves), 16 KB
+constexpr int kPBytes = kRows * 128;            // [128 rows][64 keys] bf16 = 16 KB
 constexpr int kOffK = 0;
-constexpr int kOffV = kKStages * kTileBytes;
-constexpr int kOffP = kOffV + kVStages * kTileBytes;   // [128 rows][64 keys] bf16 = 16 KB
-constexpr int kBarOff = kOffP + kRows * 128;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;
+constexpr int kOffV = kOffK + kKStages * kTileBytes;
+constexpr int kOffP = kOffV + kVStages * kTileBytes;
+constexpr int kBarOff = kOffP + kTiles * kPBufs * kPBytes;
+constexpr int kSmemBytes = kBarOff + 512 + 1024;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.f;        // log2 units
 
 struct Bars {
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t q_full, s_full, s_free, p_full, o_done, drain;
+    uint64_t q_full[kTiles], s_full[kTiles], s_free[kTiles];
+    uint64_t p_full[kTiles][kPBufs], o_done[kTiles][kPBufs];  // per P buffer: P written, P V done
+    uint64_t drain;
     uint32_t tmem_base;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 struct TcArgs {
     const __nv_bfloat16* q;
@@ -69,17 +84,38 @@ struct TcArgs {
     __nv_bfloat16* out;
     unsigned* status;
     int max_blocks, num_heads, num_kv_heads, num_blocks, group;
-    float scale_log2;
+    float scale_log2;  // |scale| log2(e)
+    int negate_q;      // scale < 0: Q enters negated
 };
 
-// Key tiles a query tile needs: keys [0, kmax) with kmax the last query's position + 1.
+// Keys a query tile needs: [0, kmax) with kmax the position of its last query + 1.
 __device__ __forceinline__ int tile_key_count(int mt, int tpt, int C, int L) {
     const int tok0 = mt * tpt;
     if (mt < 0 || tok0 >= C) return 0;
     return L - C + tok0 + min(tpt, C - tok0);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+// The two query tiles of pair p out of T: the (p+1)-th longest and the (p+1)-th shortest
+// (-1: none).  Pairs p >= ceil(T / 2) hold nothing.
+__device__ __forceinline__ void pair_tiles(int p, int T, int& t0, int& t1) {
+    t0 = -1;
+    t1 = -1;
+    if (p < 0 || 2 * p >= T) return;
+    t0 = T - 1 - p;
+    t1 = p < t0 ? p : -1;
+}
+
+__device__ __forceinline__ int pair_key_count(int p, int T, int tpt, int C, int L) {
+    int t0, t1;
+    pair_tiles(p, T, t0, t1);
+    return max(tile_key_count(t0, tpt, C, L), tile_key_count(t1, tpt, C, L));
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
                                                                  const __grid_constant__ TcArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -91,23 +127,23 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
     asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(cnum));
     const int rank = static_cast<int>(crank), csize = static_cast<int>(cnum);
     const uint16_t all_mask = static_cast<uint16_t>((1u << csize) - 1u);
-    const int mt = gridDim.x - 1 - blockIdx.x;  // the latest (longest) query tiles first
+    const int p = blockIdx.x;  // tile pair
     const int kvh = blockIdx.y, b = blockIdx.z;
     const int g = a.group, tpt = kRows / g;
     const int q0 = a.cu_q_lens[b];
     const int C = a.cu_q_lens[b + 1] - q0;
     const int L = a.seq_lens[b];
     if (C < 0 || L < C || L > a.max_blocks * kBlockSize) {  // the same for the whole cluster
-        if (threadIdx.x == 0 && mt == gridDim.x - 1 && kvh == 0) atomicOr(a.status, kDevOutOfRange);
+        if (threadIdx.x == 0 && p == 0 && kvh == 0) atomicOr(a.status, kDevOutOfRange);
         return;
     }
-    const int tok0 = mt * tpt;
-    const int ntok = tok0 < C ? min(tpt, C - tok0) : 0;
-    const int rows_valid = ntok * g;
-    const int pos0 = L - C + tok0;                          // position of the tile's first query
-    const int ntiles = (tile_key_count(mt, tpt, C, L) + kKeys - 1) / kKeys;  // this CTA's tiles
-    int kmax_cl = 0;                                        // keys any member of the cluster needs
-    for (int r = 0; r < csize; ++r) kmax_cl = max(kmax_cl, tile_key_count(mt + rank - r, tpt, C, L));
+    const int T = (C + tpt - 1) / tpt;  // query tiles of this sequence
+    int mtile[kTiles], ntiles[kTiles];
+    pair_tiles(p, T, mtile[0], mtile[1]);
+#pragma unroll
+    for (int t = 0; t < kTiles; ++t) ntiles[t] = (tile_key_count(mtile[t], tpt, C, L) + kKeys - 1) / kKeys;
+    int kmax_cl = 0;  // keys any member of the cluster needs
+    for (int r = 0; r < csize; ++r) kmax_cl = max(kmax_cl, pair_key_count(p + r - rank, T, tpt, C, L));
     const int ntiles_cl = (kmax_cl + kKeys - 1) / kKeys;
     const int nblk = (kmax_cl + kBlockSize - 1) / kBlockSize;  // pool blocks read
 
@@ -120,175 +156,180 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->v_empty[s], csize);
         }
-        mbar_init(&bars->q_full, 128);
-        mbar_init(&bars->s_full, 1);
-        mbar_init(&bars->s_free, 128);
-        mbar_init(&bars->p_full, 128);
-        mbar_init(&bars->o_done, 1);
+        for (int t = 0; t < kTiles; ++t) {
+            mbar_init(&bars->q_full[t], 128);
+            mbar_init(&bars->s_full[t], 1);
+            mbar_init(&bars->s_free[t], 128);
+            for (int s = 0; s < kPBufs; ++s) {
+                mbar_init(&bars->p_full[t][s], 128);
+                mbar_init(&bars->o_done[t][s], 1);
+            }
+        }
         mbar_init(&bars->drain, 1);
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&bars->tmem_base, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     // every member's barriers exist before any multicast box or release can reach them
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == 5) {
-        // ------------------------------------------------------------ TMA producer
-        // issue order K(0), K(1), V(0), K(2), V(1), ...: K runs one tile ahead of V.  Of the
-        // 8 boxes of a stage (4 blocks x 2 column halves) this member issues those with
+    if (warp == kKLoadWarp || warp == kVLoadWarp) {
+        // ------------------------------------------------------------ TMA producers (K, V)
+        // Of the 8 boxes of a stage (4 blocks x 2 column halves) this member issues those with
         // index % csize == rank, multicast to the whole cluster.
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
+        const bool is_k = warp == kKLoadWarp;
+        const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+        uint64_t* full = is_k ? bars->k_full : bars->v_full;
+        uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+        uint8_t* ring = smem + (is_k ? kOffK : kOffV);
+        constexpr int kStages = kKStages;
+        static_assert(kKStages == kVStages, "one ring shape for both producers");
+        if (lane == 0) prefetch_tensormap(map);
         const uint64_t pol = l2_evict_last_policy();  // prefix blocks are shared across sequences
         const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks;
         const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;  // past the pool: zero fill
         int c0 = 0;
         int cur = lane < nblk ? __ldg(bt + lane) : 0;
         int nxt = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
-        auto tile_rows = [&](int j, int (&rows)[4]) {
+        const bool my_box = lane < 8 && (lane % csize) == rank;
+        const int box_t = lane >> 1, box_h = lane & 1;
+        bool ok = true;
+        int issued = 0;
+        for (int j = 0; j < ntiles_cl && ok; ++j) {
+            // pool row of block 4j + box_t (for the issuing lanes)
             if (4 * j >= c0 + 32) {
                 c0 += 32;
                 cur = nxt;
                 nxt = c0 + 32 + lane < nblk ? __ldg(bt + c0 + 32 + lane) : 0;
             }
-            if (c0 + lane < nblk && (cur < 0 || cur >= a.num_blocks)) {
-                atomicOr(a.status, kDevOutOfRange);
-                cur = 0;
+            if (is_k && c0 + lane < nblk && (cur < 0 || cur >= a.num_blocks)) atomicOr(a.status, kDevOutOfRange);
+            if (cur < 0 || cur >= a.num_blocks) cur = 0;
+            const int lb = 4 * j + box_t;
+            const int id = __shfl_sync(0xffffffffu, cur, (lb - c0) & 31);
+            const int row = lb < nblk ? (id * a.num_kv_heads + kvh) * kBlockSize : oob_row;
+            const int s = j % kStages;
+            if (lane == 0) {
+                if (j >= kStages) ok = mbar_wait(&empty[s], ((j / kStages) & 1) ^ 1);
+                if (ok) mbar_arrive_expect_tx(&full[s], kTileBytes);
             }
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const int lb = 4 * j + t;
-                const int id = __shfl_sync(0xffffffffu, cur, (lb - c0) & 31);
-                rows[t] = lb < nblk ? (id * a.num_kv_heads + kvh) * kBlockSize : oob_row;
+            ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+            if (ok) {
+                if (my_box)
+                    tma_load_2d_mc(ring + s * kTileBytes + box_h * kHalf + box_t * 2048, map, box_h * 64, row, &full[s],
+                                   all_mask, pol);
+                ++issued;
             }
-        };
-        const bool my_box = lane < 8 && (lane % csize) == rank;
-        bool ok = true;
-        int k_issued = 0, v_issued = 0;
-        int rows_k[4], rows_v[4];
-        for (int step = 0; step <= ntiles_cl && ok; ++step) {
-            if (step < ntiles_cl) {
-                tile_rows(step, rows_k);
-                const int s = step % kKStages;
-                if (lane == 0) {
-                    if (step >= kKStages) ok = mbar_wait(&bars->k_empty[s], ((step / kKStages) & 1) ^ 1);
-                    if (ok) mbar_arrive_expect_tx(&bars->k_full[s], kTileBytes);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-                if (ok) {
-                    if (my_box) {
-                        const int t = lane >> 1, h = lane & 1;
-                        const int row = t == 0 ? rows_k[0] : t == 1 ? rows_k[1] : t == 2 ? rows_k[2] : rows_k[3];
-                        tma_load_2d_mc(smem + kOffK + s * kTileBytes + h * kHalf + t * 2048, &tm_k, h * 64, row,
-                                       &bars->k_full[s], all_mask, pol);
-                    }
-                    ++k_issued;
-                }
-            }
-            if (ok && step > 0) {
-                const int j = step - 1, s = j % kVStages;
-                if (lane == 0) {
-                    if (j >= kVStages) ok = mbar_wait(&bars->v_empty[s], ((j / kVStages) & 1) ^ 1);
-                    if (ok) mbar_arrive_expect_tx(&bars->v_full[s], kTileBytes);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-                if (ok) {
-                    if (my_box) {
-                        const int t = lane >> 1, h = lane & 1;
-                        const int row = t == 0 ? rows_v[0] : t == 1 ? rows_v[1] : t == 2 ? rows_v[2] : rows_v[3];
-                        tma_load_2d_mc(smem + kOffV + s * kTileBytes + h * kHalf + t * 2048, &tm_v, h * 64, row,
-                                       &bars->v_full[s], all_mask, pol);
-                    }
-                    ++v_issued;
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < 4; ++t) rows_v[t] = rows_k[t];
         }
         if (lane == 0) {
             // Before the CTA may leave: every stage armed here has been filled (by every
             // member's boxes), and every member has released it (so no release can still be
             // on its way to this CTA's barriers).
-            for (int j = max(0, k_issued - kKStages); j < k_issued; ++j) {
-                if (!mbar_wait(&bars->k_full[j % kKStages], (j / kKStages) & 1)) ok = false;
-                if (!mbar_wait(&bars->k_empty[j % kKStages], (j / kKStages) & 1)) ok = false;
-            }
-            for (int j = max(0, v_issued - kVStages); j < v_issued; ++j) {
-                if (!mbar_wait(&bars->v_full[j % kVStages], (j / kVStages) & 1)) ok = false;
-                if (!mbar_wait(&bars->v_empty[j % kVStages], (j / kVStages) & 1)) ok = false;
+            for (int j = max(0, issued - kStages); j < issued; ++j) {
+                if (!mbar_wait(&full[j % kStages], (j / kStages) & 1)) ok = false;
+                if (!mbar_wait(&empty[j % kStages], (j / kStages) & 1)) ok = false;
             }
             if (!ok) atomicOr(a.status, kDevTimeout);
         }
-    } else if (warp == 4) {
-        // ------------------------------------------------------------ MMA issue (one thread)
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = tc_idesc_bf16(kRows, kKeys, false);
-            constexpr uint32_t idesc_o = tc_idesc_bf16(kRows, kD, true);
-            const uint32_t p_s = smem_u32(smem + kOffP);
-            bool ok = mbar_wait(&bars->q_full, 0);
-            for (int j = 0; j <= ntiles_cl && ok; ++j) {
-                if (j < ntiles_cl) {
-                    const int s = j % kKStages;
-                    ok = mbar_wait(&bars->k_full[s], (j / kKStages) & 1);
-                    if (ok && j < ntiles) {
-                        if (j > 0) ok = mbar_wait(&bars->s_free, (j - 1) & 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint32_t k_s = smem_u32(smem + kOffK + s * kTileBytes);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issue (whole warp)
+        // per key tile j: S_0 = Q_0 K_j^T, S_1 = Q_1 K_j^T, then O_0 += P_0 V_{j-1},
+        // O_1 += P_1 V_{j-1}: each tile's Q K^T runs while the other tile's softmax does.
+        // The warp runs the loop together and one elected lane issues, so every operand is
+        // warp-uniform; waits give one verdict for the warp.
+        constexpr uint32_t idesc_s = tc_idesc_bf16(kRows, kKeys, false);
+        constexpr uint32_t idesc_o = tc_idesc_bf16(kRows, kD, true);
+        // Operand descriptors are built once; a stage, a buffer or a k-step only moves the
+        // start address, which adds (offset >> 4) to the low field (no carry: every shared
+        // address is below 2^18).
+        const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + kOffK), 0, 1024);
+        const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + kOffV), kHalf, 1024);
+        const uint64_t pdesc0 = smem_desc_sw128(smem_u32(smem + kOffP), 0, 1024);
+        bool ok = true;
 #pragma unroll
-                        for (int kk = 0; kk < kD / 16; ++kk) {
-                            const uint64_t bd = smem_desc_sw128(k_s + (kk >> 2) * kHalf + (kk & 3) * 32, 0, 1024);
-                            tc_mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, idesc_s, kk > 0 ? 1u : 0u);
-                        }
-                        tc_commit(&bars->s_full);
-                    }
+        for (int t = 0; t < kTiles; ++t)
+            if (ok && ntiles[t] > 0) ok = mbar_wait_warp(&bars->q_full[t], 0);
+        int ks_ = 0, kph = 0, vs_ = 0, vph = 0;  // ring slot and phase of K(j) and V(j-1)
+        for (int j = 0; j <= ntiles_cl && ok; ++j) {
+            if (j < ntiles_cl) {
+                ok = mbar_wait_warp(&bars->k_full[ks_], kph);
+                const uint64_t kd = kdesc0 + (uint64_t)((ks_ * kTileBytes) >> 4);
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t) {
+                    if (!ok || j >= ntiles[t]) continue;
+                    if (j > 0) ok = mbar_wait_warp(&bars->s_free[t], (j - 1) & 1);
                     if (!ok) break;
-                    tc_commit_mc(&bars->k_empty[s], all_mask);  // release the K slot cluster-wide
+                    tc_fence_after();
+                    const uint32_t tm_s = tmem + t * kTmemTile + kTmemS, tm_q = tmem + t * kTmemTile + kTmemQ;
+#pragma unroll
+                    for (int kk = 0; kk < kD / 16; ++kk)
+                        tc_mma_ts_ew(tm_s, tm_q + kk * 8, kd + (uint64_t)(((kk >> 2) * kHalf + (kk & 3) * 32) >> 4),
+                                     idesc_s, kk > 0 ? 1u : 0u);
+                    tc_commit_ew(&bars->s_full[t]);
                 }
-                if (j > 0) {
-                    const int jp = j - 1, s = jp % kVStages;
-                    ok = mbar_wait(&bars->v_full[s], (jp / kVStages) & 1);
-                    if (ok && jp < ntiles) {
-                        ok = mbar_wait(&bars->p_full, jp & 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint32_t v_s = smem_u32(smem + kOffV + s * kTileBytes);
-#pragma unroll
-                        for (int ks = 0; ks < kKeys / 16; ++ks) {
-                            const uint64_t ad = smem_desc_sw128(p_s + ks * 32, 0, 1024);
-                            const uint64_t bd = smem_desc_sw128(v_s + ks * 16 * 128, kHalf, 1024);
-                            tc_mma(tmem + kTmemO, ad, bd, idesc_o, (jp > 0 || ks > 0) ? 1u : 0u);
-                        }
-                        tc_commit(&bars->o_done);
-                    }
-                    if (!ok) break;
-                    tc_commit_mc(&bars->v_empty[s], all_mask);
+                if (!ok) break;
+                tc_commit_mc_ew(&bars->k_empty[ks_], all_mask);  // release the K slot cluster-wide
+                if (++ks_ == kKStages) {
+                    ks_ = 0;
+                    kph ^= 1;
                 }
             }
-            // every MMA issued above has finished before the tensor memory is released
-            tc_commit(&bars->drain);
-            if (!mbar_wait(&bars->drain, 0)) ok = false;
-            if (!ok) atomicOr(a.status, kDevTimeout);
+            if (j > 0) {
+                const int jp = j - 1, pb = jp & (kPBufs - 1);
+                ok = mbar_wait_warp(&bars->v_full[vs_], vph);
+                const uint64_t vd = vdesc0 + (uint64_t)((vs_ * kTileBytes) >> 4);
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t) {
+                    if (!ok || jp >= ntiles[t]) continue;
+                    ok = mbar_wait_warp(&bars->p_full[t][pb], (jp / kPBufs) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t pd = pdesc0 + (uint64_t)(((t * kPBufs + pb) * kPBytes) >> 4);
+                    const uint32_t tm_o = tmem + t * kTmemTile + kTmemO;
+                    tc_mma_ew(tm_o, pd, vd, idesc_o, jp > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int ks = 1; ks < kKeys / 16; ++ks)
+                        tc_mma_ew(tm_o, pd + (uint64_t)((ks * 32) >> 4), vd + (uint64_t)((ks * 16 * 128) >> 4), idesc_o,
+                                  1u);
+                    tc_commit_ew(&bars->o_done[t][pb]);
+                }
+                if (!ok) break;
+                tc_commit_mc_ew(&bars->v_empty[vs_], all_mask);
+                if (++vs_ == kVStages) {
+                    vs_ = 0;
+                    vph ^= 1;
+                }
+            }
         }
-        __syncwarp();
+        // every MMA issued above has finished before the tensor memory is released
+        tc_commit_ew(&bars->drain);
+        if (!mbar_wait_warp(&bars->drain, 0)) ok = false;
+        if (!ok && lane == 0) atomicOr(a.status, kDevTimeout);
     } else {
         // ------------------------------------------------------------ softmax: one row per thread
-        const int r = threadIdx.x;  // TMEM lane r, MMA row r
-        const bool valid = r < rows_valid;
+        const int t = warp >> 2;                    // query tile of this warpgroup
+        const int r = threadIdx.x & (kRows - 1);    // TMEM lane r, MMA row r
+        const int mt = t == 0 ? mtile[0] : mtile[1], nt = t == 0 ? ntiles[0] : ntiles[1];
+        const int tok0 = mt * tpt;
+        const int ntok = (mt >= 0 && tok0 < C) ? min(tpt, C - tok0) : 0;
+        const bool valid = r < ntok * g;
         const int qi = r / g, h = r % g;
-        const int pos = valid ? pos0 + qi : -1;  // causal limit of the row (inclusive)
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        {
-            // Q row -> TMEM columns [64, 128) as bf16 pairs (zeros for rows past the chunk)
+        const int pos = valid ? L - C + tok0 + qi : -1;  // causal limit of the row (inclusive)
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t tm_row = tmem + lane_base + t * kTmemTile;
+        // this warpgroup zeroes V rows past the sequence end in key tile j unless tile 0 of
+        // this CTA computes j too (it does so first: the MMA thread issues tile 0's P V first)
+        const int zero_from = t == 0 ? 0 : ntiles[0];
+        if (nt > 0) {
+            // Q row -> TMEM columns [64, 128) as bf16 pairs (zeros for rows past the chunk).
+            // A negative scale is carried by negating Q (exact in bf16), so the kernel works
+            // with |scale| and the row maximum of the raw scores.
+            const uint32_t sign = a.negate_q ? 0x80008000u : 0u;
             const uint4* src = reinterpret_cast<const uint4*>(
                 a.q + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD);
 #pragma unroll
@@ -297,116 +338,155 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const uint4 v = valid ? __ldg(src + half * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
-                    w[4 * c] = v.x;
-                    w[4 * c + 1] = v.y;
-                    w[4 * c + 2] = v.z;
-                    w[4 * c + 3] = v.w;
+                    w[4 * c] = v.x ^ sign;
+                    w[4 * c + 1] = v.y ^ sign;
+                    w[4 * c + 2] = v.z ^ sign;
+                    w[4 * c + 3] = v.w ^ sign;
                 }
-                tmem_st32(tmem + lane_base + kTmemQ + half * 32, w);
+                tmem_st32(tm_row + kTmemQ + half * 32, w);
             }
             tc_fence_before();
-            mbar_arrive(&bars->q_full);
+            mbar_arrive(&bars->q_full[t]);
         }
-        uint8_t* prow = smem + kOffP;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < ntiles; ++j) {
-            if (!mbar_wait(&bars->s_full, j & 1)) {
+        // tcgen05.ld / tcgen05.st are warp-collective: every decision that leads to one (a wait
+        // that gave up, a rescale of O) is taken by the whole warp.
+        for (int j = 0; j < nt; ++j) {
+            if (__any_sync(0xffffffffu, !mbar_wait(&bars->s_full[t], j & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             uint32_t sr[2][32];
-            tmem_ld32(tmem + lane_base + kTmemS, sr[0]);
-            tmem_ld32(tmem + lane_base + kTmemS + 32, sr[1]);
+            tmem_ld64(tm_row + kTmemS, sr[0], sr[1]);
             tc_fence_before();
-            mbar_arrive(&bars->s_free);
+            mbar_arrive(&bars->s_free[t]);
 
             const int k0 = j * kKeys;
-            const bool need_mask = k0 + kKeys - 1 > pos;
-            float x[kKeys];
-            float mx = -INFINITY;
+            const int lim = pos - k0;  // keys c <= lim of this tile are visible to the row
+            float sv[kKeys];
 #pragma unroll
-            for (int c = 0; c < kKeys; ++c) {
-                const float v = __uint_as_float(sr[c >> 5][c & 31]) * a.scale_log2;
-                x[c] = (need_mask && k0 + c > pos) ? -INFINITY : v;
-                mx = fmaxf(mx, x[c]);
-            }
-            const float m_new = fmaxf(m_used, mx);
-            const bool rescale = m_new > m_used + kRescaleThreshold;  // always for the first visible key
-            if (j > 0) {
-                // PV(j-1) has finished: O is stable and the P buffer is free (every phase, in order)
-                if (!mbar_wait(&bars->o_done, (j - 1) & 1)) {
-                    ok = false;
-                    break;
+            for (int c = 0; c < kKeys; ++c) sv[c] = __uint_as_float(sr[c >> 5][c & 31]);
+            // Row maximum of the raw scores (|scale| keeps the order), in independent chains:
+            // one row per thread leaves no other parallelism to hide a long dependent chain.
+            // Tiles wholly below the diagonal need no mask; only they are common.
+            float mx;
+            if (lim >= kKeys - 1) {
+                float m4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) m4[e] = fmaxf(sv[2 * e], sv[2 * e + 1]);
+#pragma unroll
+                for (int c = 8; c < kKeys; c += 8) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) m4[e] = fmax3(m4[e], sv[c + 2 * e], sv[c + 2 * e + 1]);
                 }
-                tc_fence_after();
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            } else {
+                mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < kKeys; ++c)
+                    if (c <= lim) mx = fmaxf(mx, sv[c]);
+            }
+            const float mxs = mx == -INFINITY ? -INFINITY : mx * a.scale_log2;  // log2 units
+            const float m_new = fmaxf(m_used, mxs);
+            const bool rescale = m_new > m_used + kRescaleThreshold;  // always for the first visible key
+            const int pb = j % kPBufs;
+            // P buffer pb was last read by P V(j-2); O is only touched here when it must be
+            // rescaled, and then P V(j-1) must have finished too.  A buffer's barrier cannot
+            // run two phases ahead of these waits: P V(j) needs P(j) first.
+            const bool warp_rescale = __any_sync(0xffffffffu, rescale && m_used != -INFINITY);
+            bool wait_ok = true;
+            if (j >= kPBufs) wait_ok = mbar_wait(&bars->o_done[t][pb], ((j - kPBufs) / kPBufs) & 1);
+            if (warp_rescale && j >= 1)
+                wait_ok = mbar_wait(&bars->o_done[t][(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1) && wait_ok;
+            if (__any_sync(0xffffffffu, !wait_ok)) {
+                ok = false;
+                break;
+            }
+            if (j >= 1) tc_fence_after();
+            // alpha = 2^(m_old - m_new) for rows that re-base (0 while nothing was visible), else 1
+            const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
+            if (warp_rescale) {
+#pragma unroll
+                for (int c = 0; c < kD; c += 32) {
+                    uint32_t o[32];
+                    tmem_ld32(tm_row + kTmemO + c, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(tm_row + kTmemO + c, o);
+                }
             }
             if (rescale) {
-                const float alpha = fast_exp2(m_used - m_new);
-                if (m_used != -INFINITY) {
-#pragma unroll
-                    for (int c = 0; c < kD; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + lane_base + kTmemO + c, o);
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(tmem + lane_base + kTmemO + c, o);
-                    }
-                }
                 l *= alpha;
                 m_used = m_new;
             }
-            const float base = m_used == -INFINITY ? 0.f : m_used;
-            float lsum = 0.f;
+            const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+            uint8_t* prow = smem + kOffP + (t * kPBufs + pb) * kPBytes;
+            // p = 2^(s |scale| log2(e) - m): one packed multiply-add per two keys, then the
+            // special-function unit; sums in four packed chains.
+            float ls[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ls[e] = 0.f;
+            const bool masked = lim < kKeys - 1;
 #pragma unroll
             for (int cc = 0; cc < kKeys / 8; ++cc) {
-                float p[8];
+                float pp[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p[e] = fast_exp2(x[cc * 8 + e] - base);
-                    lsum += p[e];
+                for (int e = 0; e < 8; e += 2) {
+                    float x0, x1;
+                    fma_x2(x0, x1, sv[cc * 8 + e], sv[cc * 8 + e + 1], a.scale_log2, a.scale_log2, nbase, nbase);
+                    pp[e] = fast_exp2(x0);
+                    pp[e + 1] = fast_exp2(x1);
                 }
+                if (masked) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (cc * 8 + e > lim) pp[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) add_x2(ls[e], ls[e + 1], pp[e], pp[e + 1]);
                 uint4 v;
-                v.x = pack_bf16x2(p[0], p[1]);
-                v.y = pack_bf16x2(p[2], p[3]);
-                v.z = pack_bf16x2(p[4], p[5]);
-                v.w = pack_bf16x2(p[6], p[7]);
+                v.x = pack_bf16x2(pp[0], pp[1]);
+                v.y = pack_bf16x2(pp[2], pp[3]);
+                v.z = pack_bf16x2(pp[4], pp[5]);
+                v.w = pack_bf16x2(pp[6], pp[7]);
                 *reinterpret_cast<uint4*>(prow + swz128(r, cc)) = v;
             }
-            l += lsum;
-            if (k0 + kKeys > L) {
+            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            if (k0 + kKeys > L && j >= zero_from) {
                 // keys at or past the sequence end: zero their V rows, whatever the slots hold.
-                // V(j) has landed: PV(j-2), the previous user of this slot, finished before
-                // PV(j-1), so only this phase of the slot's barrier can be pending.  (The other
-                // members need these rows zeroed too and zero them themselves: every member
-                // that computes tile j reaches this point before releasing the slot.)
+                // Once V(j) has landed, every earlier reader of the slot has finished (its
+                // refill waited for all of them), and P V(j) of either tile is issued after
+                // this warpgroup's P(j) is complete.  (Every cluster member zeroes its own
+                // copy before releasing the slot.)
                 const int s = j % kVStages;
-                if (!mbar_wait(&bars->v_full[s], (j / kVStages) & 1)) {
+                if (__any_sync(0xffffffffu, !mbar_wait(&bars->v_full[s], (j / kVStages) & 1))) {
                     ok = false;
                     break;
                 }
                 uint8_t* vt = smem + kOffV + s * kTileBytes;
                 const int z0 = max(0, L - k0);
                 const int nchunks = (kKeys - z0) * 16;  // 16-byte chunks over both column halves
-                for (int c = r; c < nchunks; c += 128) {
+                for (int c = r; c < nchunks; c += kRows) {
                     const int row = z0 + (c >> 4), half = (c >> 3) & 1, cc = c & 7;
                     *reinterpret_cast<uint4*>(vt + half * kHalf + row * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars->p_full);
+            mbar_arrive(&bars->p_full[t][pb]);
         }
-        if (ok && ntiles > 0) ok = mbar_wait(&bars->o_done, (ntiles - 1) & 1);
-        if (ok && ntiles > 0) {
+        if (ok && nt > 0)
+            ok = !__any_sync(0xffffffffu, !mbar_wait(&bars->o_done[t][(nt - 1) % kPBufs], ((nt - 1) / kPBufs) & 1));
+        if (ok && nt > 0) {
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             __nv_bfloat16* dst = a.out + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD;
 #pragma unroll
             for (int c = 0; c < kD; c += 32) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_base + kTmemO + c, o);
+                tmem_ld32(tm_row + kTmemO + c, o);
                 if (valid) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 8) {
@@ -424,12 +504,12 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const __grid_co
         tc_fence_before();
     }
     __syncthreads();
-    if (warp == 4) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
     // no member leaves while another may still multicast into its memory or release to it
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    cluster_sync_all();
 }
 
 }  // namespace
@@ -462,18 +542,20 @@ cudaError_t launch_prefill_tc(const PoolView& pool, const AttnArgs& a, cudaStrea
     t.num_kv_heads = pool.num_kv_heads;
     t.num_blocks = pool.num_blocks;
     t.group = a.num_heads / pool.num_kv_heads;
-    t.scale_log2 = a.scale * kLog2e;
+    t.scale_log2 = std::fabs(a.scale) * kLog2e;
+    t.negate_q = a.scale < 0.f ? 1 : 0;
     const int tpt = kRows / t.group;
     const int tiles = std::max(1, (a.max_chunk + tpt - 1) / tpt);
-    // cluster over consecutive query tiles of one (sequence, kv head): up to 4 members
+    const int pairs = (tiles + 1) / 2;
+    // cluster over consecutive tile pairs of one (sequence, kv head): up to 4 members
     static const int forced = [] {
         const char* e = std::getenv("PA_PREFILL_CLUSTER");
         return e ? std::atoi(e) : 0;
     }();
     int cs = forced > 0 ? forced : 4;
     cs = std::max(1, std::min(cs, 8));
-    while (cs > 1 && cs > tiles) cs >>= 1;
-    const int gx = (tiles + cs - 1) / cs * cs;
+    while (cs > 1 && cs > pairs) cs >>= 1;
+    const int gx = (pairs + cs - 1) / cs * cs;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(gx, pool.num_kv_heads, a.batch);
     cfg.blockDim = dim3(kThreads);

@@ -242,3 +242,21 @@ def test_prefill_golden_causal_chunk():
     case = G.build(spec)
     g = GpuCase(case, append=False)
     compare(g.prefill(), G.expected(spec), spec["name"])
+
+
+@pytest.mark.parametrize("scale", [-0.09, 0.0, 0.3])
+@pytest.mark.parametrize("d", [64, 128])
+def test_scale_sign_and_zero(scale, d):
+    """A negative, zero or large softmax scale: zero gives the mean of the visible values,
+    a negative scale weights the least similar keys most."""
+    case = W.random_case(5200 + d, batch=3, num_heads=16, num_kv_heads=4, head_dim=d, min_len=1, max_len=180,
+                         q_len=40, prefill=True, shared_prefix_tokens=16, scale=scale)
+    g = GpuCase(case)
+    compare(g.prefill(), oracle_prefill(case), f"prefill scale {scale} d {d}")
+    dec = W.random_case(5300 + d, batch=3, num_heads=16, num_kv_heads=4, head_dim=d, min_len=1, max_len=400,
+                        scale=scale)
+    gd = GpuCase(dec)
+    compare(gd.decode(), oracle_decode(dec), f"decode scale {scale} d {d}")
+    ws_o, ws_lse = gd.splitkv(4)
+    compare(pa.pa_combine(ws_o, ws_lse), oracle_decode(dec), f"split-KV scale {scale} d {d}")
+    check_status_clean("scale sweep")
