@@ -5,13 +5,15 @@ One step = one pass of every call of the hot path over its workload, inputs resi
 in HBM:
   1. pa_kv_append        64 new tokens            (batched decode: 64 seqs, ctx ~U[1024,1152], 32q/8kv/128)
   2. pa_decode           batched decode, 64 seqs  (same)
-  3. pa_decode_splitkv   4 x 8192, P=8  + pa_combine   (Qwen3-32B-shaped 64q/8kv/128)
-  4. pa_decode_splitkv   1 x 32768, P=32 + pa_combine
+  3. pa_decode_splitkv   4 x 8192, P in 8..32 + pa_combine   (Qwen3-32B-shaped 64q/8kv/128)
+  4. pa_decode_splitkv   1 x 32768, P in 8..32 + pa_combine
   5. pa_kv_append        8 x 256 chunk tokens     (chunked prefill over a shared 768-token prefix)
   6. pa_prefill_chunked  8 x 256-token causal chunks, 32q/8kv/128
-value = KV bytes the attention calls must read per step / step time (GB/s), L2 flushed
-(a 512 MB buffer is read) before every timed step.  Each call is also timed on its own
-stream with CUDA events and reported under "per_call".  The two latency-bound decode
+The step is captured once as a CUDA graph and replayed, as a serving loop replays its
+decode step.  value = KV bytes the attention calls must read per step / step time (GB/s),
+L2 flushed (a 512 MB buffer is read) before every timed replay, outside the timed interval.
+Each call is also captured and timed on its own and reported under "per_call".  The
+end-to-end number ("e2e") calls the public API eagerly with host buffers.  The two latency-bound decode
 shapes (1 seq x 37 tokens, 4q/1kv/64; 1 seq x 1152 tokens, 32q/8kv/128) are reported
 under "latency" (cold and CUDA-graph-replayed).
 
@@ -286,23 +288,51 @@ def flush_l2(buf):
     return buf.sum()
 
 
-def time_steps(step, steps, warmup, flush_buf):
-    n = len(step.calls)
+def capture_graph(fn, dev):
+    """fn's launches as one CUDA graph (captured on a side stream after one eager run)."""
+    st = torch.cuda.Stream(device=dev)
+    st.wait_stream(torch.cuda.current_stream(dev))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        fn()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(graph, stream=st):
+            fn()
+    torch.cuda.current_stream(dev).wait_stream(st)
+    torch.cuda.synchronize(dev)
+    return graph
+
+
+def time_graph(graph, reps, flush_buf):
+    """Device time of `reps` replays, each after an L2 flush that stays outside the interval."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for s, e in ev:
+        flush_l2(flush_buf)
+        s.record()
+        graph.replay()
+        e.record()
+    torch.cuda.synchronize()
+    return np.array([s.elapsed_time(e) * 1e3 for s, e in ev])  # us
+
+
+def time_steps(step, steps, warmup, flush_buf, dev):
+    """The step is replayed as one CUDA graph (as a serving loop replays its decode step):
+    `steps` timed replays after `warmup` untimed ones.  Per-call times come from one graph
+    per call, timed the same way, and attribute the step's time to its calls."""
+    graph = capture_graph(step.run, dev)
     for _ in range(warmup):
         flush_l2(flush_buf)
-        step.run()
+        graph.replay()
     torch.cuda.synchronize()
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(steps)]
-    for k in range(steps):
-        flush_l2(flush_buf)
-        evs[k][0].record()
-        step.run(evs[k])
-    torch.cuda.synchronize()
-    per_call = np.zeros((steps, n))
-    for k in range(steps):
-        for i in range(n):
-            per_call[k, i] = evs[k][i].elapsed_time(evs[k][i + 1]) * 1e3  # us
-    return per_call
+    step_us = time_graph(graph, steps, flush_buf)
+    per_call = np.zeros((steps, len(step.calls)))
+    for i, (_, _, fn, _, _) in enumerate(step.calls):
+        g1 = capture_graph(fn, dev)
+        time_graph(g1, 2, flush_buf)
+        per_call[:, i] = time_graph(g1, steps, flush_buf)
+        del g1
+    del graph
+    return step_us, per_call
 
 
 def time_e2e(step, steps, flush_buf):
@@ -445,7 +475,8 @@ def dist_setup():
 
 def base_config():
     return {"workload": WORKLOAD, "l2": "flushed before every timed step (512 MB buffer read)",
-            "timing": "CUDA events on the launching stream around every call; step = sum"}
+            "timing": "CUDA events around each replay of the step captured as one CUDA graph; per-call "
+                      "times from one graph per call, timed the same way"}
 
 
 def run_reference(args, ws, rank):
@@ -514,7 +545,7 @@ def main(argv=None):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.time()
-    per_call = time_steps(step, args.steps, args.warmup, flush_buf)
+    step_us, per_call = time_steps(step, args.steps, args.warmup, flush_buf, dev)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -524,7 +555,6 @@ def main(argv=None):
     if status:
         raise RuntimeError(f"device status {status:#x} after the timed steps")
 
-    step_us = per_call.sum(axis=1)
     mean_step_us = float(step_us.mean())
     if ws > 1:
         t = torch.tensor([mean_step_us], device=dev)

@@ -186,8 +186,9 @@ size_t pa_noalloc_scratch_bytes(void);
 int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
 
 /*
- * Partition count suggested for pa_decode_splitkv on the current device: a power of two
- * (1..64) that fills one wave of the GPU's SMs while keeping >= 8 blocks per partition.
+ * Partition count suggested for pa_decode_splitkv on the current device (1..64): the
+ * largest count whose CTAs (batch x num_kv_heads x count) fit one wave of four per SM,
+ * keeping >= 8 blocks per partition.
  */
 int pa_splitkv_num_partitions(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
 

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
                                                         const int64_t* __restrict__ slots, long long per_tensor,
                                                         int num_kv_heads, int chunks, long long pool_slots,
                                                         unsigned* status) {
+    pdl_trigger();
+    pdl_wait();
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * per_tensor; i += stride) {
         const bool is_v = i >= per_tensor;
@@ -54,11 +56,16 @@ cudaError_t launch_kv_append(const PoolView& pool, const void* k_new, const void
     const long long per_tensor = (long long)num_tokens * pool.num_kv_heads * chunks;
     const long long want = (2 * per_tensor + 255) / 256;
     const int blocks = static_cast<int>(std::max(1LL, std::min<long long>(want, (long long)device_info().num_sms * 16)));
-    kv_append_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint4*>(pool.k), static_cast<uint4*>(pool.v),
-                                                 static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new),
-                                                 slots, per_tensor, pool.num_kv_heads, chunks,
-                                                 (long long)pool.num_blocks * kBlockSize, status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<uint4*>(pool.k), static_cast<uint4*>(pool.v),
+                              static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, per_tensor,
+                              pool.num_kv_heads, chunks, (long long)pool.num_blocks * kBlockSize, status);
 }
 
 }  // namespace pa

@@ -82,6 +82,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     const int split = blockIdx.x, nsplit = gridDim.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = a.group;
+    pdl_trigger();
+    pdl_wait();
 
     int L = a.seq_lens[b];
     if (L < 0 || L > a.max_blocks * kBlockSize) {
@@ -282,6 +284,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const float
     __shared__ float dpart[kCombineWarps];
     const int r = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
     const float* lse = ws_lse + (size_t)r * P;
     float M = -INFINITY;
     for (int p = lane; p < P; p += 32) M = fmaxf(M, __ldg(lse + p));
@@ -379,14 +383,15 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cuda
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Sh::smem_bytes(da.stages);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (!SPLIT && nsplit > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = nsplit;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = nsplit;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     return cudaLaunchKernelEx(&cfg, kern, pool.tile_k, pool.tile_v, da);
 }
@@ -448,11 +453,13 @@ int decode_splits_for(int batch, int num_kv_heads, int max_blocks) {
 }
 
 int splitkv_partitions_for(int batch, int num_kv_heads, int max_blocks) {
-    // a power of two that fills one wave of four CTAs per SM, keeping >= 8 blocks per partition
+    // The partitions of all (sequence, kv head) pairs fill one wave of four CTAs per SM as
+    // evenly as possible (an SM holding one CTA more than its neighbours finishes last),
+    // keeping >= 8 blocks per partition; at most 64.
     const int items = std::max(1, batch * num_kv_heads);
-    const int want = std::max(1, (4 * device_info().num_sms) / items);
-    int p = 1;
-    while (p * 2 <= want && p * 2 <= 64 && (max_blocks / (p * 2)) >= 8) p *= 2;
+    int p = std::max(1, (4 * device_info().num_sms) / items);
+    p = std::min(p, 64);
+    while (p > 1 && max_blocks / p < 8) --p;
     return p;
 }
 
@@ -469,10 +476,15 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_lse, int batch, in
                            int num_partitions, void* out, cudaStream_t stream) {
     const int rows = batch * num_heads;
     auto* o = static_cast<__nv_bfloat16*>(out);
-    if (head_dim == 128)
-        combine_kernel<128><<<rows, kCombineWarps * 32, 0, stream>>>(ws_o, ws_lse, num_partitions, o);
-    else
-        combine_kernel<64><<<rows, kCombineWarps * 32, 0, stream>>>(ws_o, ws_lse, num_partitions, o);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows);
+    cfg.blockDim = dim3(kCombineWarps * 32);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (head_dim == 128) return cudaLaunchKernelEx(&cfg, combine_kernel<128>, ws_o, ws_lse, num_partitions, o);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<64>, ws_o, ws_lse, num_partitions, o);
     return cudaGetLastError();
 }
 

@@ -79,6 +79,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return true;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels launched with programmatic stream serialization may start while the previous
+// kernel in the stream is finishing.  Every kernel here lets its successor launch at once
+// (pdl_trigger) and waits for its predecessor's completion and memory (pdl_wait) before it
+// touches global memory.  Both are no-ops for an ordinary launch.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA
 // 2-D tiled load of one box into shared memory, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,

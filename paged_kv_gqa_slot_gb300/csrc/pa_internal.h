@@ -54,6 +54,15 @@ struct AttnArgs {
 const DeviceInfo& device_info();
 unsigned* device_status_ptr();
 
+// Launch attribute that lets a kernel overlap its launch with the previous kernel's tail
+// (the kernel itself waits for that kernel before touching memory).
+inline cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute at = {};
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    return at;
+}
+
 cudaError_t launch_kv_append(const PoolView& pool, const void* k_new, const void* v_new, const int64_t* slots,
                              int num_tokens, unsigned* status, cudaStream_t stream);
 cudaError_t launch_decode(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);

@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const __grid_cons
 
     const int mt = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
     const int g = a.group;
     const int q0 = a.cu_q_lens[b];
     const int C = a.cu_q_lens[b + 1] - q0;
@@ -172,8 +174,15 @@ cudaError_t launch_mma(const PoolView& pool, const AttnArgs& a, cudaStream_t str
     const long long rows = (long long)a.max_chunk * pa_.group;
     const int tiles = static_cast<int>((rows + kRows - 1) / kRows);
     dim3 grid(std::max(1, tiles), pool.num_kv_heads, a.batch);
-    kern<<<grid, kThreads, Sh::kSmemBytes, stream>>>(pool.tile_k, pool.tile_v, pa_);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Sh::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, pool.tile_k, pool.tile_v, pa_);
 }
 
 }  // namespace

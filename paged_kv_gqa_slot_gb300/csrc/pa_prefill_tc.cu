@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const uint16_t all_mask = static_cast<uint16_t>((1u << csize) - 1u);
     const int p = blockIdx.x;  // tile pair
     const int kvh = blockIdx.y, b = blockIdx.z;
+    pdl_trigger();
+    pdl_wait();
     const int g = a.group, tpt = kRows / g;
     const int q0 = a.cu_q_lens[b];
     const int C = a.cu_q_lens[b + 1] - q0;
@@ -561,13 +563,13 @@ cudaError_t launch_prefill_tc(const PoolView& pool, const AttnArgs& a, cudaStrea
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cs;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, pool.tm_k, pool.tm_v, t);
 }
 
