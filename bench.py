@@ -3,8 +3,8 @@
 
 One step = one pass of every call of the hot path over its workload, inputs resident
 in HBM:
-  1. pa_kv_append        64 new tokens            (batched decode: 64 seqs, ctx ~U[1024,1152], 32q/8kv/128)
-  2. pa_decode           batched decode, 64 seqs  (same)
+  1-2. pa_append_decode  append of 64 new tokens fused with the batched decode (64 seqs,
+                         ctx ~U[1024,1152], 32q/8kv/128): pa_kv_append + pa_decode in one launch
   3. pa_decode_splitkv   4 x 8192, P in 8..32 + pa_combine   (Qwen3-32B-shaped 64q/8kv/128)
   4. pa_decode_splitkv   1 x 32768, P in 8..32 + pa_combine
   5. pa_kv_append        8 x 256 chunk tokens     (chunked prefill over a shared 768-token prefix)
@@ -43,7 +43,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "paged GQA decode: KV GB/s & frac of GB300 HBM peak; µs/call per batch×ctx"
-WORKLOAD = ("serving step: append(64) + decode 64x~1088 (32q/8kv/128) + split-KV 4x8192 and 1x32768 (P in 8..32) "
+WORKLOAD = ("serving step: fused append(64)+decode 64x~1088 (32q/8kv/128) + split-KV 4x8192 and 1x32768 (P in 8..32) "
             "with combine (64q/8kv/128) + append(2048) + chunked prefill 8x256 over a shared 768-token "
             "prefix (32q/8kv/128); block 16; bf16 N(0,1)")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -212,12 +212,12 @@ class Step:
                                                                                c.scale, g["out"])),
                                    attn_bytes(c), "bytes"))
         if g3 is not None:
+            # the decode step's append and attention in one launch (pa_append_decode)
             self.calls += [
-                ("kv_append[batched_decode,64]", "append",
-                 lambda: pa.pa_kv_append(g3["pool"], g3["k_new"], g3["v_new"], g3["slots"]), app_bytes(c3), "bytes"),
-                ("decode[batched_decode,64x~1088]", "decode",
-                 lambda: pa.pa_decode(g3["pool"], g3["q"], g3["bt"], g3["sl"], c3.scale, g3["out"]),
-                 attn_bytes(c3), "bytes")]
+                ("append_decode[batched_decode,64x~1088]", "decode",
+                 lambda: pa.pa_append_decode(g3["pool"], g3["k_new"], g3["v_new"], g3["slots"], g3["q"], g3["bt"],
+                                             g3["sl"], c3.scale, g3["out"]),
+                 attn_bytes(c3) + app_bytes(c3), "bytes")]
         if g4a is not None:
             self.calls += [
                 (f"decode_splitkv[4x8192,P={self.P4a}]", "splitkv",

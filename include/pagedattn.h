@@ -102,6 +102,24 @@ int pa_decode(const pa_pool *pool, const void *q, const int32_t *block_tables, i
               pa_stream_t stream);
 
 /*
+ * pa_append_decode -- pa_kv_append of one new row per sequence followed by pa_decode, in
+ * one launch (a decode step's append and attention fused; the pages' engines write a
+ * token's K/V and then attend over it in every full-attention layer).  Equivalent to
+ *   pa_kv_append(pool, k_new, v_new, slot_mapping, batch); pa_decode(pool, q, ...);
+ * on the same stream, given that slot_mapping[b] is the slot of token seq_lens[b] - 1 of
+ * sequence b (block_tables[b][(seq_lens[b]-1)/16] * 16 + (seq_lens[b]-1) % 16), as an
+ * append for that token must be.
+ *   k_new, v_new   [batch, num_kv_heads, head_dim] bf16, 16-byte aligned: the new rows
+ *   slot_mapping   [batch] int64; < 0 skips the write (the decode then reads whatever the
+ *                  slot holds).  Any other slot than the one above is not written and sets
+ *                  PA_DEV_OUT_OF_RANGE.
+ * Other arguments, errors and results as pa_decode.
+ */
+int pa_append_decode(const pa_pool *pool, const void *k_new, const void *v_new, const int64_t *slot_mapping,
+                     const void *q, const int32_t *block_tables, int32_t max_blocks, const int32_t *seq_lens,
+                     int32_t batch, int32_t num_heads, float scale, void *out, pa_stream_t stream);
+
+/*
  * Workspace of pa_decode_splitkv, in bytes: ws_o [batch, num_heads, P, head_dim] fp32
  * followed by ws_lse [batch, num_heads, P] fp32 (ws_lse may live anywhere 16-byte aligned;
  * this is their sum).  Host-only, no CUDA call.

@@ -20,7 +20,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_decode_splitkv", "pa_combine", "pa_prefill_chunked",
+__all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_append_decode", "pa_decode_splitkv", "pa_combine", "pa_prefill_chunked",
            "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "pa_splitkv_num_partitions",
            "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes", "PagedAttnError",
            "library", "library_path", "BLOCK_SIZE", "EXPORTED_SYMBOLS"]
@@ -28,7 +28,7 @@ __all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_decode_splitkv", "pa_combi
 BLOCK_SIZE = 16
 PKG = Path(__file__).resolve().parent
 _LIB_PATH = PKG / "libpagedattn.so"
-EXPORTED_SYMBOLS = ("pa_kv_append", "pa_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv", "pa_combine",
+EXPORTED_SYMBOLS = ("pa_kv_append", "pa_decode", "pa_append_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv", "pa_combine",
                     "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_splitkv_num_partitions",
                     "pa_status_str", "pa_version", "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes")
 
@@ -75,6 +75,7 @@ def library() -> ctypes.CDLL:
     sig = {
         "pa_kv_append": (ctypes.c_int, [pool, P, P, P, I32, P]),
         "pa_decode": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, P, P]),
+        "pa_append_decode": (ctypes.c_int, [pool, P, P, P, P, P, I32, P, I32, I32, F32, P, P]),
         "pa_splitkv_workspace_bytes": (SZ, [I32, I32, I32, I32]),
         "pa_decode_splitkv": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, I32, P, P, P]),
         "pa_combine": (ctypes.c_int, [P, P, I32, I32, I32, I32, P, P]),
@@ -159,6 +160,21 @@ def pa_decode(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor, seq_len
                              block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale),
                              _dev(out, torch.bfloat16, "out"), _stream(stream))
     _check(rc, "pa_decode")
+    return out
+
+
+def pa_append_decode(pool: PaPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                     q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """pa_kv_append of one new row per sequence followed by pa_decode, in one launch."""
+    B, Hq, _ = q.shape
+    out = torch.empty_like(q) if out is None else out
+    rc = library().pa_append_decode(pool.ref, _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
+                                    _dev(slot_mapping, torch.int64, "slot_mapping"), _dev(q, torch.bfloat16, "q"),
+                                    _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
+                                    _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale),
+                                    _dev(out, torch.bfloat16, "out"), _stream(stream))
+    _check(rc, "pa_append_decode")
     return out
 
 

@@ -221,6 +221,33 @@ int pa_decode(const pa_pool* pool, const void* q, const int32_t* block_tables, i
     return from_cuda(launch_decode(v, a, (cudaStream_t)stream));
 }
 
+int pa_append_decode(const pa_pool* pool, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                     const void* q, const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                     int32_t batch, int32_t num_heads, float scale, void* out, pa_stream_t stream) {
+    PoolView v;
+    int rc = check_attn(pool, &v, q, block_tables, max_blocks, seq_lens, batch, num_heads, scale, out);
+    if (rc || batch == 0) return rc;
+    if (num_heads / v.num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
+    if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
+    rc = check_pool(pool, &v, true);
+    if (rc) return rc;
+    AttnArgs a{};
+    a.q = q;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.status = device_status_ptr();
+    if (!a.status) return PA_ERR_CUDA;
+    a.batch = batch;
+    a.num_heads = num_heads;
+    a.max_blocks = max_blocks;
+    a.scale = scale;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.slots = slot_mapping;
+    return from_cuda(launch_decode(v, a, (cudaStream_t)stream));
+}
+
 size_t pa_splitkv_workspace_bytes(int32_t batch, int32_t num_heads, int32_t head_dim, int32_t num_partitions) {
     if (batch < 0 || num_heads < 0 || head_dim < 0 || num_partitions < 0) return 0;
     const size_t rows = (size_t)batch * num_heads * num_partitions;

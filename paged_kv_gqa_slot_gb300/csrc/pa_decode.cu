@@ -66,6 +66,11 @@ struct DecodeArgs {
     int max_blocks, num_heads, num_kv_heads, num_blocks, group;
     int stages;  // ring slots, a multiple of kConsumerWarps
     float scale_log2;
+    const uint4* k_new;  // fused append (decode only): [B, Hkv, D] bf16, or null
+    const uint4* v_new;
+    const int64_t* slots;  // [B]
+    void* k_pool;  // the pool, for the fused append's row write
+    void* v_pool;
 };
 
 template <int D, int NT, bool SPLIT>
@@ -82,7 +87,6 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     const int split = blockIdx.x, nsplit = gridDim.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = a.group;
-    pdl_trigger();
     pdl_wait();
 
     int L = a.seq_lens[b];
@@ -94,6 +98,32 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     const int per = (nb + nsplit - 1) / nsplit;
     const int blk0 = split * per;
     const int n = max(0, min(per, nb - blk0));
+
+    if (a.k_new != nullptr && warp == 0 && nb > 0 && blk0 + n == nb && n > 0) {
+        // Fused append: the CTA that reads the sequence's last block first writes the new K/V
+        // row of its kv head into the slot (token L-1 of the sequence), so the result equals an
+        // append followed by the decode.  The row must land in that very slot; any other slot
+        // is reported and not written.  The proxy fence and the barrier below order the write
+        // before this CTA's TMA loads of the block.
+        const int64_t slot = a.slots[b];
+        if (slot >= 0) {
+            const int lb = (L - 1) / kBlockSize, off = (L - 1) % kBlockSize;
+            const int32_t blk = a.block_tables[(size_t)b * a.max_blocks + lb];
+            const bool ok_slot = blk >= 0 && blk < a.num_blocks && slot == (int64_t)blk * kBlockSize + off;
+            constexpr int kChunks = D * 2 / 16;  // 16-byte chunks of one row
+            if (!ok_slot) {
+                if (lane == 0) atomicOr(a.status, kDevOutOfRange);
+            } else if (lane < 2 * kChunks) {
+                const int c = lane % kChunks;
+                const bool is_v = lane >= kChunks;
+                const size_t src = ((size_t)b * a.num_kv_heads + kvh) * kChunks + c;
+                const size_t dst = (((size_t)blk * a.num_kv_heads + kvh) * kBlockSize + off) * kChunks + c;
+                uint4* pool = static_cast<uint4*>(is_v ? a.v_pool : a.k_pool);
+                pool[dst] = __ldg((is_v ? a.v_new : a.k_new) + src);
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+            }
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -148,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             }
     }
     __syncthreads();  // ring drained: every issued copy has landed and been consumed
+    pdl_trigger();    // the next kernel may launch while this one merges and writes
 
     // ---- per-warp partials -> one CTA partial (unnormalised O, max m, sum l per head)
     float* part = reinterpret_cast<float*>(smem);
@@ -377,6 +408,11 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cuda
     da.group = a.num_heads / pool.num_kv_heads;
     da.scale_log2 = a.scale * kLog2e;
     da.stages = stages_for<D>(nsplit * pool.num_kv_heads * a.batch);
+    da.k_new = static_cast<const uint4*>(a.k_new);
+    da.v_new = static_cast<const uint4*>(a.v_new);
+    da.slots = a.slots;
+    da.k_pool = pool.k;
+    da.v_pool = pool.v;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nsplit, pool.num_kv_heads, a.batch);

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cstdlib>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,17 +50,28 @@ struct AttnArgs {
     int num_partitions;          // split-KV only
     int max_chunk;               // prefill only
     float scale;
+    // decode only, fused append (null: none): one new K/V row per sequence [B, Hkv, D] bf16
+    // and its slot [B]; written by the kernel before it reads the sequence's last block
+    const void* k_new;
+    const void* v_new;
+    const int64_t* slots;
 };
 
 const DeviceInfo& device_info();
 unsigned* device_status_ptr();
 
 // Launch attribute that lets a kernel overlap its launch with the previous kernel's tail
-// (the kernel itself waits for that kernel before touching memory).
+// (the kernel itself waits for that kernel before touching memory).  Off unless PA_PDL=1:
+// on the benchmark step it measured 2-4 us slower per step than plain stream order (the
+// early-launched CTAs hold SM slots while they wait).
 inline cudaLaunchAttribute pdl_attribute() {
+    static const int allowed = [] {
+        const char* e = std::getenv("PA_PDL");
+        return (e && e[0] == '1') ? 1 : 0;
+    }();
     cudaLaunchAttribute at = {};
     at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at.val.programmaticStreamSerializationAllowed = 1;
+    at.val.programmaticStreamSerializationAllowed = allowed;
     return at;
 }
 

@@ -129,7 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const uint16_t all_mask = static_cast<uint16_t>((1u << csize) - 1u);
     const int p = blockIdx.x;  // tile pair
     const int kvh = blockIdx.y, b = blockIdx.z;
-    pdl_trigger();
     pdl_wait();
     const int g = a.group, tpt = kRows / g;
     const int q0 = a.cu_q_lens[b];
@@ -506,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc_fence_before();
     }
     __syncthreads();
+    pdl_trigger();  // the next kernel may launch while this CTA leaves
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);

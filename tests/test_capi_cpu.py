@@ -103,5 +103,11 @@ def test_validation_rejects_before_launch(lib):
     assert lib.pa_decode_splitkv_noalloc(P(_pool(d=96)), FAKE, FAKE, 4, FAKE, 1, 4, 0.1, 8, FAKE, None) == \
         pa.PA_ERR_UNSUPPORTED
     assert lib.pa_decode_splitkv_noalloc(P(ok_pool), FAKE, FAKE, 4, FAKE, 0, 4, 0.1, 8, FAKE, None) == pa.PA_OK
+    # fused append + decode: missing rows, batch 0, head dim outside the compiled set
+    assert lib.pa_append_decode(P(ok_pool), None, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 1, 4, 0.1, FAKE, None) == \
+        pa.PA_ERR_INVALID_ARG
+    assert lib.pa_append_decode(P(ok_pool), FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 0, 4, 0.1, FAKE, None) == pa.PA_OK
+    assert lib.pa_append_decode(P(_pool(d=96)), FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, 1, 4, 0.1, FAKE, None) == \
+        pa.PA_ERR_UNSUPPORTED
     # status needs a flags pointer
     assert lib.pa_device_status(None, 1, None) == pa.PA_ERR_INVALID_ARG

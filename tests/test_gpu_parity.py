@@ -260,3 +260,57 @@ def test_scale_sign_and_zero(scale, d):
     ws_o, ws_lse = gd.splitkv(4)
     compare(pa.pa_combine(ws_o, ws_lse), oracle_decode(dec), f"split-KV scale {scale} d {d}")
     check_status_clean("scale sweep")
+
+
+FUSED_CASES = {
+    # one CTA per (sequence, kv head)
+    "batched_decode": lambda: W.batched_decode(),
+    # one sequence: split over a 16-CTA cluster, the last member owns the new token's block
+    "one_seq_cluster": lambda: W.random_case(5400, batch=1, num_heads=32, num_kv_heads=8, head_dim=128,
+                                             min_len=1100, max_len=1200),
+    # d = 64, single kv head, tokens landing at every offset of a block
+    "tiny_d64": lambda: W.random_case(5401, batch=6, num_heads=4, num_kv_heads=1, head_dim=64, min_len=1, max_len=40),
+    # group 8, ragged lengths
+    "g8_ragged": lambda: W.random_case(5402, batch=5, num_heads=64, num_kv_heads=8, head_dim=128, min_len=1,
+                                       max_len=700),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FUSED_CASES))
+def test_append_decode_fused(name):
+    """pa_append_decode equals pa_kv_append then pa_decode: the pool afterwards is
+    bit-identical to the oracle's append, the output matches the oracle's decode."""
+    case = FUSED_CASES[name]()
+    assert list(case.q_lens) == [1] * case.batch and case.k_new.shape[0] == case.batch
+    g = GpuCase(case, append=False)  # the new rows' slots still hold NaN
+    out = pa.pa_append_decode(g.pool, g.k_new, g.v_new, g.slots, g.q, g.bt, g.sl, case.scale)
+    check_status_clean(f"fused {name}")
+    k_ref, v_ref = oracle_pool(case)
+    assert np.array_equal(u16(g.k.cpu()), k_ref) and np.array_equal(u16(g.v.cpu()), v_ref), "pool after fused append"
+    compare(out, oracle_decode(case), f"fused append+decode {name}")
+
+
+def test_append_decode_slot_checks():
+    """A skipped slot (< 0) is not written; a slot that is not token seq_len-1 of its sequence
+    is reported (PA_DEV_OUT_OF_RANGE) and not written; the other sequences are unaffected."""
+    case = W.random_case(5403, batch=4, num_heads=32, num_kv_heads=8, head_dim=128, min_len=20, max_len=300)
+    g = GpuCase(case, append=False)
+    slots = g.slots.clone()
+    good0, good1 = int(slots[0]), int(slots[1])
+    slots[0] = -1                        # skip
+    slots[1] = good1 + 1 if good1 % 16 != 15 else good1 - 1  # a neighbouring slot: wrong token
+    k_before = u16(g.k.cpu()).copy()
+    out = pa.pa_append_decode(g.pool, g.k_new, g.v_new, slots, g.q, g.bt, g.sl, case.scale)
+    flags = pa.pa_device_status(clear=True)
+    assert flags == pa.PA_DEV_OUT_OF_RANGE, f"status {flags:#x}"
+    k_after = u16(g.k.cpu())
+    def rows(slot):
+        blk, off = divmod(slot, 16)
+        return k_after[blk, :, off, :], k_before[blk, :, off, :]
+    for s in (good0, good1, int(slots[1])):
+        after, before = rows(s)
+        assert np.array_equal(after, before), f"slot {s} written"
+    # sequences 2 and 3 were appended and decoded normally
+    k_ref, v_ref = oracle_pool(case)
+    ref = oracle_decode(case, (k_ref, v_ref))
+    compare(out[2:], ref[2:], "fused, untouched sequences")
