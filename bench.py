@@ -401,6 +401,19 @@ def latency_configs(flush_buf):
                      "kv_gbs_cold": round(kvb / float(np.median(cold)) / 1e3, 1),
                      "decode_splits": pa.pa_decode_num_splits(c.batch, c.num_kv_heads, c.max_blocks)}
         del graph
+    # multi-query decode: 64 sequences x 4 draft tokens (a speculative-decoding verify)
+    c = W.spec_verify()
+    k, v = c.k_cache.cuda(), c.v_cache.cuda()
+    pool = pa.PaPool(k, v)
+    pa.pa_kv_append(pool, c.k_new.cuda(), c.v_new.cuda(), c.slot_mapping.cuda())
+    q, bt, sl, cu = c.q.cuda(), c.block_tables.cuda(), c.seq_lens.cuda(), c.cu_q_lens.cuda()
+    out = torch.empty_like(q)
+    fn = lambda: pa.pa_prefill_chunked(pool, q, cu, bt, sl, c.scale, 4, out)
+    fn()
+    torch.cuda.synchronize()
+    us = float(np.median(time_graph(capture_graph(fn, q.device), 20, flush_buf)))
+    res["spec_verify[64x~1088,C=4,32q/8kv/128]"] = {"us_per_call": round(us, 2),
+                                                   "kv_gbs": round(c.kv_bytes() / us / 1e3, 1)}
     return res
 
 

@@ -285,6 +285,25 @@ __device__ __forceinline__ void load_q_heads(uint32_t (&qb)[NT][D / 16][2], cons
     }
 }
 
+// Multi-query form: column n is (query n / g, head n % g) of a chunk of C queries starting at
+// token q0 of the q tensor (rows >= C * g are zero).
+template <int D, int NT>
+__device__ __forceinline__ void load_q_rows(uint32_t (&qb)[NT][D / 16][2], const __nv_bfloat16* q, int q0, int C,
+                                            int g, int num_heads, int kvh) {
+    const int lane = threadIdx.x & 31, c = (lane & 3) * 2;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + (lane >> 2);
+        const __nv_bfloat16* row =
+            n < C * g ? q + ((size_t)(q0 + n / g) * num_heads + (size_t)kvh * g + n % g) * D : nullptr;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            qb[nt][kk][0] = row ? ld_u32(row + kk * 16 + c) : 0u;
+            qb[nt][kk][1] = row ? ld_u32(row + kk * 16 + c + 8) : 0u;
+        }
+    }
+}
+
 // One head column's update from this thread's two tokens (x0: token lane/4, x8: lane/4+8);
 // returns alpha and writes the two probabilities back into x0, x8.
 __device__ __forceinline__ float head_update(float& m, float& l, float& x0, float& x8) {
@@ -306,10 +325,14 @@ __device__ __forceinline__ float head_update(float& m, float& l, float& x0, floa
 //   ot[nt][mt][4]: O^T accumulators, d = mt*16 + lane/4 (+8), head nt*8 + 2*(lane%4) (+1)
 //   valid        : keys with in-block index < valid exist (the rest are masked and their
 //                  V rows zeroed in the fragments, whatever the slot holds)
-template <int D, int NT>
+// With MQ the columns are the (query, head) rows of a multi-query chunk: column j of this
+// thread in n-tile nt sees keys up to absolute position colpos[nt][j] (causal), and the
+// block's first key is at kbase.
+template <int D, int NT, bool MQ = false>
 __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const uint32_t (&qb)[NT][D / 16][2],
                                                  float (&ot)[NT][D / 16][4], HeadState<NT>& hs, int valid,
-                                                 float scale_log2) {
+                                                 float scale_log2, const int (*colpos)[2] = nullptr,
+                                                 int kbase = 0) {
     const int lane = threadIdx.x & 31;
     const int mi = lane >> 3, rr = lane & 7;
     const int ltok = rr + ((mi & 1) << 3);  // K matrices 0,2: tokens 0-7; 1,3: tokens 8-15
@@ -330,8 +353,16 @@ __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const
     uint32_t pb[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        float xa0 = v0 ? st[nt][0] * scale_log2 : -INFINITY, xa8 = v8 ? st[nt][2] * scale_log2 : -INFINITY;
-        float xb0 = v0 ? st[nt][1] * scale_log2 : -INFINITY, xb8 = v8 ? st[nt][3] * scale_log2 : -INFINITY;
+        bool va0 = v0, va8 = v8, vb0 = v0, vb8 = v8;
+        if (MQ) {
+            const int la = colpos[nt][0] - kbase, lb = colpos[nt][1] - kbase;
+            va0 = t0 <= la;
+            va8 = t0 + 8 <= la;
+            vb0 = t0 <= lb;
+            vb8 = t0 + 8 <= lb;
+        }
+        float xa0 = va0 ? st[nt][0] * scale_log2 : -INFINITY, xa8 = va8 ? st[nt][2] * scale_log2 : -INFINITY;
+        float xb0 = vb0 ? st[nt][1] * scale_log2 : -INFINITY, xb8 = vb8 ? st[nt][3] * scale_log2 : -INFINITY;
         const float aa = head_update(hs.m[nt][0], hs.l[nt][0], xa0, xa8);
         const float ab = head_update(hs.m[nt][1], hs.l[nt][1], xb0, xb8);
 #pragma unroll

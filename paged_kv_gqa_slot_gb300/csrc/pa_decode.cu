@@ -69,11 +69,12 @@ struct DecodeArgs {
     const uint4* k_new;  // fused append (decode only): [B, Hkv, D] bf16, or null
     const uint4* v_new;
     const int64_t* slots;  // [B]
+    const int32_t* cu_q_lens;  // multi-query: chunk of query tokens of each sequence [B+1]
     void* k_pool;  // the pool, for the fused append's row write
     void* v_pool;
 };
 
-template <int D, int NT, bool SPLIT>
+template <int D, int NT, bool SPLIT, bool MQ>
 __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                           const __grid_constant__ CUtensorMap tm_v,
                                                           const __grid_constant__ DecodeArgs a) {
@@ -94,10 +95,23 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         if (threadIdx.x == 0) atomicOr(a.status, kDevOutOfRange);
         L = L < 0 ? 0 : a.max_blocks * kBlockSize;
     }
+    // Multi-query (MQ): the last C tokens of the sequence are queries (a short causal chunk,
+    // e.g. the draft tokens of a speculative-decoding verify); the MMA columns are its C x g
+    // (query, head) rows.  Otherwise one query, the g heads.
+    int C = 1, q0 = b;
+    if (MQ) {
+        q0 = a.cu_q_lens[b];
+        C = a.cu_q_lens[b + 1] - q0;
+        if (C < 0 || C > L || C * g > 8 * NT) {
+            if (threadIdx.x == 0) atomicOr(a.status, kDevOutOfRange);
+            C = 0;
+        }
+    }
+    const int R = MQ ? C * g : g;  // columns in use
     const int nb = (L + kBlockSize - 1) / kBlockSize;
     const int per = (nb + nsplit - 1) / nsplit;
     const int blk0 = split * per;
-    const int n = max(0, min(per, nb - blk0));
+    const int n = R == 0 ? 0 : max(0, min(per, nb - blk0));
 
     if (a.k_new != nullptr && warp == 0 && nb > 0 && blk0 + n == nb && n > 0) {
         // Fused append: the CTA that reads the sequence's last block first writes the new K/V
@@ -152,7 +166,19 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
                                           a.num_kv_heads, kvh, a.status, l2_evict_first_policy());
     } else {
         uint32_t qb[NT][D / 16][2];
-        load_q_heads<D, NT>(qb, a.q + ((size_t)b * a.num_heads + (size_t)kvh * g) * D, g);
+        int colpos[NT][2];  // MQ: causal limit of this thread's two columns per n-tile
+        if (MQ) {
+            load_q_rows<D, NT>(qb, a.q, q0, C, g, a.num_heads, kvh);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int col = nt * 8 + (lane & 3) * 2 + j;
+                    colpos[nt][j] = col < R ? L - C + col / g : -1;
+                }
+        } else {
+            load_q_heads<D, NT>(qb, a.q + ((size_t)b * a.num_heads + (size_t)kvh * g) * D, g);
+        }
         bool ok = true;
         for (int i = warp; i < n; i += kConsumerWarps) {
             const int st = i % stages;
@@ -161,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             uint8_t* kt = smem + st * KvTile<D>::kStageBytes;
             uint8_t* vt = kt + KvTile<D>::kTileBytes;
             const int valid = min(kBlockSize, L - (blk0 + i) * kBlockSize);
-            block_step_heads<D, NT>(smem_u32(kt), smem_u32(vt), qb, ot, hs, valid, a.scale_log2);
+            block_step_heads<D, NT, MQ>(smem_u32(kt), smem_u32(vt), qb, ot, hs, valid, a.scale_log2, colpos,
+                                        (blk0 + i) * kBlockSize);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
         }
@@ -207,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         }
     }
     __syncthreads();
-    const int E = g * D;
+    const int E = R * D;
     for (int e = threadIdx.x; e < E; e += kThreads) {
         const int h = e / D;
         float M = -INFINITY;
@@ -243,11 +270,16 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         }
         return;
     }
-    __nv_bfloat16* outg = a.out + ((size_t)b * a.num_heads + (size_t)kvh * g) * D;
+    // element e = row * D + d of this CTA's output -> its place in out
+    auto out_at = [&](int e) -> __nv_bfloat16* {
+        const int row = e / D;
+        const size_t tok = MQ ? (size_t)q0 + row / g : (size_t)b;
+        return a.out + (tok * a.num_heads + (size_t)kvh * g + (MQ ? row % g : row)) * D + e % D;
+    };
     if (nsplit == 1) {
         for (int e = threadIdx.x; e < E; e += kThreads) {
             const float den = cta[16 + e / D];
-            outg[e] = __float2bfloat16_rn(den > 0.f ? cta[32 + e] / den : 0.f);
+            *out_at(e) = __float2bfloat16_rn(den > 0.f ? cta[32 + e] / den : 0.f);
         }
         return;
     }
@@ -259,14 +291,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     float* wgt = part;  // [nsplit][16] merge weights, then den[16] (the warp partials are done)
     float* den = part + 16 * 16;
     const int rank = static_cast<int>(cluster.block_rank());
-    for (int t = threadIdx.x; t < nsplit * g; t += kThreads) {
-        const int r = t / g, h = t % g;
+    for (int t = threadIdx.x; t < nsplit * R; t += kThreads) {
+        const int r = t / R, h = t % R;
         const float* rc = cluster.map_shared_rank(cta, r);
         wgt[r * 16 + h] = rc[h];
         wgt[256 + 32 + r * 16 + h] = rc[16 + h];
     }
     __syncthreads();
-    if (threadIdx.x < g) {
+    if (threadIdx.x < R) {
         const int h = threadIdx.x;
         float M = -INFINITY;
         for (int r = 0; r < nsplit; ++r) M = fmaxf(M, wgt[r * 16 + h]);
@@ -294,8 +326,9 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             acc.w += w * v.w;
         }
         const float inv = den[h] > 0.f ? 1.f / den[h] : 0.f;
-        *reinterpret_cast<__nv_bfloat162*>(outg + e) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-        *reinterpret_cast<__nv_bfloat162*>(outg + e + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        __nv_bfloat16* dst = out_at(e);  // 4 consecutive d of one row (D is a multiple of 4)
+        *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
     }
     cluster.sync();  // keep this CTA's partial alive until every reader is done
 }
@@ -374,10 +407,10 @@ int stages_for(int /*ctas*/) {
     return D == 128 ? 6 : 12;
 }
 
-template <int D, int NT, bool SPLIT>
+template <int D, int NT, bool SPLIT, bool MQ = false>
 cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cudaStream_t stream) {
     using Sh = DecodeShape<D>;
-    auto kern = decode_kernel<D, NT, SPLIT>;
+    auto kern = decode_kernel<D, NT, SPLIT, MQ>;
     static bool configured = false;  // per instantiation; attribute setting is idempotent
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -413,6 +446,7 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cuda
     da.slots = a.slots;
     da.k_pool = pool.k;
     da.v_pool = pool.v;
+    da.cu_q_lens = MQ ? a.cu_q_lens : nullptr;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(nsplit, pool.num_kv_heads, a.batch);
@@ -436,10 +470,10 @@ template <bool SPLIT>
 cudaError_t dispatch(const PoolView& pool, const AttnArgs& a, int nsplit, cudaStream_t stream) {
     const int g = a.num_heads / pool.num_kv_heads;
     if (pool.head_dim == 128)
-        return g > 8 ? launch_one<128, 2, SPLIT>(pool, a, nsplit, stream)
-                     : launch_one<128, 1, SPLIT>(pool, a, nsplit, stream);
-    return g > 8 ? launch_one<64, 2, SPLIT>(pool, a, nsplit, stream)
-                 : launch_one<64, 1, SPLIT>(pool, a, nsplit, stream);
+        return g > 8 ? launch_one<128, 2, SPLIT, false>(pool, a, nsplit, stream)
+                     : launch_one<128, 1, SPLIT, false>(pool, a, nsplit, stream);
+    return g > 8 ? launch_one<64, 2, SPLIT, false>(pool, a, nsplit, stream)
+                 : launch_one<64, 1, SPLIT, false>(pool, a, nsplit, stream);
 }
 
 int max_cluster_splits() {
@@ -447,7 +481,7 @@ int max_cluster_splits() {
     static int cached = 0;
     if (cached) return cached;
     int best = 8;
-    auto kern = decode_kernel<128, 1, false>;
+    auto kern = decode_kernel<128, 1, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              DecodeShape<128>::smem_bytes(DecodeShape<128>::kMaxStages)) == cudaSuccess) {
@@ -502,6 +536,19 @@ int splitkv_partitions_for(int batch, int num_kv_heads, int max_blocks) {
 cudaError_t launch_decode(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
     const int nsplit = decode_splits_for(a.batch, pool.num_kv_heads, a.max_blocks);
     return dispatch<false>(pool, a, nsplit, stream);
+}
+
+bool decode_mq_supported(int group, int max_chunk) { return max_chunk >= 1 && (long long)max_chunk * group <= 16; }
+
+cudaError_t launch_decode_mq(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
+    const int g = a.num_heads / pool.num_kv_heads;
+    const int nsplit = decode_splits_for(a.batch, pool.num_kv_heads, a.max_blocks);
+    const bool two = a.max_chunk * g > 8;
+    if (pool.head_dim == 128)
+        return two ? launch_one<128, 2, false, true>(pool, a, nsplit, stream)
+                   : launch_one<128, 1, false, true>(pool, a, nsplit, stream);
+    return two ? launch_one<64, 2, false, true>(pool, a, nsplit, stream)
+               : launch_one<64, 1, false, true>(pool, a, nsplit, stream);
 }
 
 cudaError_t launch_decode_splitkv(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {

@@ -79,6 +79,10 @@ cudaError_t launch_kv_append(const PoolView& pool, const void* k_new, const void
                              int num_tokens, unsigned* status, cudaStream_t stream);
 cudaError_t launch_decode(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_decode_splitkv(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
+// Multi-query decode: a chunk of <= max_chunk queries per sequence over its cache, on the
+// decode kernel (columns = query x head), when max_chunk x group <= 16.
+bool decode_mq_supported(int group, int max_chunk);
+cudaError_t launch_decode_mq(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, int batch, int num_heads, int head_dim,
                            int num_partitions, void* out, cudaStream_t stream);
 cudaError_t launch_prefill(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);

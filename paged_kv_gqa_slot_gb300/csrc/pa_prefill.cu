@@ -16,6 +16,7 @@
 // block that lies wholly past its last row's causal limit, so the diagonal costs only
 // the masking of the blocks it straddles.
 #include <algorithm>
+#include <cstdlib>
 
 #include "pa_block_attn.cuh"
 #include "pa_internal.h"
@@ -188,7 +189,17 @@ cudaError_t launch_mma(const PoolView& pool, const AttnArgs& a, cudaStream_t str
 }  // namespace
 
 cudaError_t launch_prefill(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
-    if (prefill_tc_supported(pool.head_dim, a.num_heads / pool.num_kv_heads)) return launch_prefill_tc(pool, a, stream);
+    const int g = a.num_heads / pool.num_kv_heads;
+    // A chunk of a few queries (a speculative-decoding verify, one decode token) is a
+    // bandwidth-bound decode with a causal mask: it runs on the decode kernel, its
+    // (query, head) rows on the MMA N dimension.  PA_PREFILL_IMPL=t or m forces the
+    // tensor-core or warp-MMA prefill kernels instead, for A/B comparisons.
+    static const char forced = [] {
+        const char* e = std::getenv("PA_PREFILL_IMPL");
+        return e ? e[0] : '\0';
+    }();
+    if (forced != 't' && forced != 'm' && decode_mq_supported(g, a.max_chunk)) return launch_decode_mq(pool, a, stream);
+    if (prefill_tc_supported(pool.head_dim, g)) return launch_prefill_tc(pool, a, stream);
     if (pool.head_dim == 128) return launch_mma<128>(pool, a, stream);
     return launch_mma<64>(pool, a, stream);
 }

@@ -314,3 +314,33 @@ def test_append_decode_slot_checks():
     k_ref, v_ref = oracle_pool(case)
     ref = oracle_decode(case, (k_ref, v_ref))
     compare(out[2:], ref[2:], "fused, untouched sequences")
+
+
+@pytest.mark.parametrize("hq,hkv,d,q_len,shared", [(32, 8, 128, 4, 0), (32, 8, 128, 3, 32), (64, 8, 128, 2, 0),
+                                                   (16, 4, 64, 4, 16), (4, 4, 64, 16, 0), (8, 8, 128, 16, 0)])
+def test_multi_query_decode(hq, hkv, d, q_len, shared):
+    """Chunks of a few queries (the shape of a speculative-decoding verify) with
+    chunk x group <= 16 run on the decode kernel, their (query, head) rows on the MMA N
+    dimension with a causal mask per column; ragged chunk lengths, chunks that start
+    anywhere inside a block, a shared prefix."""
+    case = W.random_case(5500 + hq + hkv + d + q_len + shared, batch=6, num_heads=hq, num_kv_heads=hkv,
+                         head_dim=d, min_len=1 + shared, max_len=300, q_len=q_len, prefill=True,
+                         shared_prefix_tokens=shared)
+    assert max(case.q_lens) * (hq // hkv) <= 16
+    g = GpuCase(case)
+    compare(g.prefill(), oracle_prefill(case), f"multi-query {hq}/{hkv}/{d} C<={q_len}")
+    check_status_clean("multi-query decode")
+
+
+def test_multi_query_decode_cluster_and_empty_chunk():
+    """One long sequence (split over a CTA cluster) with a 4-query chunk, and a batch in
+    which one sequence has an empty chunk and another is all chunk (C == seq_len)."""
+    c1 = W.paged_case(name="mq_cluster", seed=5510, seq_lens=[1131], q_lens=[4], new_lens=[4], num_heads=32,
+                      num_kv_heads=8, head_dim=128, num_blocks=4096)
+    g1 = GpuCase(c1)
+    compare(g1.prefill(), oracle_prefill(c1), "multi-query over a cluster")
+    c2 = W.paged_case(name="mq_empty", seed=5511, seq_lens=[40, 3, 18, 77], q_lens=[0, 3, 2, 4],
+                      new_lens=[0, 3, 2, 4], num_heads=16, num_kv_heads=4, head_dim=128, num_blocks=64)
+    g2 = GpuCase(c2)
+    compare(g2.prefill(), oracle_prefill(c2), "multi-query with an empty chunk")
+    check_status_clean("multi-query cluster / empty chunk")

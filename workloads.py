@@ -235,6 +235,17 @@ def batched_decode(seed: int = 1003, batch: int = 64) -> PagedCase:
                       num_blocks=16384, gen=gen)
 
 
+def spec_verify(seed: int = 1006, batch: int = 64, drafts: int = 4) -> PagedCase:
+    """The batched-decode shape with `drafts` query tokens per sequence instead of one (a
+    speculative-decoding verify: the last `drafts` tokens of each sequence are appended and
+    attend causally), 32/8/128, context ~U[1024, 1152], 16384-block pool."""
+    gen = generator(seed)
+    lens = torch.randint(1024, 1153, (batch,), generator=gen).tolist()
+    return paged_case(name="spec_verify", seed=seed, seq_lens=lens, q_lens=[drafts] * batch,
+                      new_lens=[drafts] * batch, num_heads=32, num_kv_heads=8, head_dim=128,
+                      num_blocks=16384, gen=gen)
+
+
 def splitkv_decode(seed: int = 1004, batch: int = 4, context: int = 8192) -> PagedCase:
     """Qwen3-32B-shaped long-context decode, 64/8/128 (group 8), 4096-block pool."""
     return paged_case(name=f"splitkv_{batch}x{context}", seed=seed, seq_lens=[context] * batch,
