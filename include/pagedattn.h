@@ -54,7 +54,8 @@ enum pa_status {
     PA_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed */
     PA_ERR_OUT_OF_RANGE = -4, /* pa_device_status: a block id / slot / length outside the pool was skipped */
     PA_ERR_TIMEOUT = -5,      /* pa_device_status: a pipeline wait ran out (a bug, never expected) */
-    PA_ERR_TOO_LARGE = -6     /* pa_decode_splitkv_noalloc: the request does not fit its static scratch */
+    PA_ERR_TOO_LARGE = -6,    /* pa_decode_splitkv_noalloc: the request does not fit its static scratch */
+    PA_ERR_REJECTED = -7      /* pa_bm_admit: the request's whole lifetime does not fit the pool */
 };
 
 /* Device status bits reported by pa_device_status. */
@@ -209,6 +210,63 @@ int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks
  * keeping >= 8 blocks per partition.
  */
 int pa_splitkv_num_partitions(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
+
+/* ------------------------------------------------------------------------------------
+ * Host-side KV block manager (no GPU involved).  "Qwen3-4B / 8B / 32B", "Architecture
+ * Notes": the paged KV cache uses full-lifetime admission (a request that cannot fit is
+ * rejected rather than left to hang under memory pressure) and a prefix cache, on by
+ * default; "Qwen3-32B Serving Load": the KV budget is profiled at load (21.4 GB, 5360
+ * blocks); "Warm Prefix-Cache TTFT": a warm request computes only what its cached prompt
+ * prefix does not cover.
+ *
+ * Bytes of one block (K and V of every layer): num_layers * 2 * num_kv_heads * block_size
+ * * head_dim * dtype_bytes.  Qwen3-32B (64 layers, 8 kv heads, d 128, bf16, 16-token blocks)
+ * gives 4 MiB, so 5360 blocks are 22.48 GB (20.94 GiB).  0 on a non-positive argument.
+ */
+int64_t pa_kv_block_bytes(int32_t num_layers, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t dtype_bytes);
+/* Blocks a budget of budget_bytes holds (floor). */
+int32_t pa_kv_budget_blocks(int64_t budget_bytes, int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t dtype_bytes);
+
+/* Opaque manager of num_blocks pool blocks of block_size tokens; thread-safe.  NULL on a
+ * bad argument or no memory.  Destroy with pa_bm_destroy. */
+typedef struct pa_blockmgr pa_blockmgr;
+pa_blockmgr *pa_bm_create(int32_t num_blocks, int32_t block_size, int32_t enable_prefix_cache);
+void pa_bm_destroy(pa_blockmgr *bm);
+
+/*
+ * Admit request_id with its prompt tokens[0, n_tokens) and at most max_new_tokens tokens to
+ * generate.  The blocks for its whole lifetime (n_tokens + max_new_tokens) are reserved now,
+ * or nothing is and PA_ERR_REJECTED is returned.  With the prefix cache, the prompt's leading
+ * full blocks whose token ids (and every token before them) match a cached block are shared
+ * instead of reserved; at least the prompt's last token is always left to compute.
+ *   block_table      out: the request's block ids, in token order (table_cap entries or more)
+ *   n_blocks         out: ceil((n_tokens + max_new_tokens) / block_size)
+ *   n_cached_tokens  out: prompt tokens whose K/V is already in the pool (a multiple of
+ *                    block_size); compute tokens [n_cached_tokens, n_tokens) next.
+ * PA_ERR_INVALID_ARG on a bad argument or a request id already admitted.
+ */
+int pa_bm_admit(pa_blockmgr *bm, int64_t request_id, const int32_t *tokens, int32_t n_tokens,
+                int32_t max_new_tokens, int32_t *block_table, int32_t table_cap, int32_t *n_blocks,
+                int32_t *n_cached_tokens);
+
+/*
+ * Append n_new generated tokens to the request's token list (within its reserved lifetime)
+ * and declare that the K/V of its first `computed` tokens is now in the pool.  Blocks that
+ * are full within those tokens enter the prefix cache (one entry per distinct content).
+ */
+int pa_bm_commit(pa_blockmgr *bm, int64_t request_id, const int32_t *new_tokens, int32_t n_new, int32_t computed);
+
+/* Release the request: its blocks lose a user; cached ones stay reusable until the allocator
+ * needs them (the one released longest ago first), the rest are free at once. */
+int pa_bm_release(pa_blockmgr *bm, int64_t request_id);
+
+/* Pool slots of the request's tokens [start, start + n): the slot_mapping of pa_kv_append. */
+int pa_bm_slots(pa_blockmgr *bm, int64_t request_id, int32_t start, int32_t n, int64_t *slots);
+
+/* Free (never used or uncached), cached-but-idle, and in-use block counts (any may be NULL). */
+int pa_bm_stats(pa_blockmgr *bm, int32_t *free_blocks, int32_t *cached_idle_blocks, int32_t *used_blocks);
 
 /* Human-readable name of a status code (static string). */
 const char *pa_status_str(int status);

@@ -23,6 +23,7 @@ import torch
 __all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_append_decode", "pa_decode_splitkv", "pa_combine", "pa_prefill_chunked",
            "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "pa_splitkv_num_partitions",
            "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes", "PagedAttnError",
+           "BlockManager", "pa_kv_block_bytes", "pa_kv_budget_blocks",
            "library", "library_path", "BLOCK_SIZE", "EXPORTED_SYMBOLS"]
 
 BLOCK_SIZE = 16
@@ -30,10 +31,13 @@ PKG = Path(__file__).resolve().parent
 _LIB_PATH = PKG / "libpagedattn.so"
 EXPORTED_SYMBOLS = ("pa_kv_append", "pa_decode", "pa_append_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv", "pa_combine",
                     "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_splitkv_num_partitions",
-                    "pa_status_str", "pa_version", "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes")
+                    "pa_status_str", "pa_version", "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes",
+                    "pa_kv_block_bytes", "pa_kv_budget_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_admit",
+                    "pa_bm_commit", "pa_bm_release", "pa_bm_slots", "pa_bm_stats")
 
 PA_OK = 0
 PA_ERR_INVALID_ARG = -1
+PA_ERR_REJECTED = -7
 PA_ERR_UNSUPPORTED = -2
 PA_ERR_CUDA = -3
 PA_ERR_OUT_OF_RANGE = -4
@@ -86,6 +90,15 @@ def library() -> ctypes.CDLL:
         "pa_decode_splitkv_noalloc": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, I32, P, P]),
         "pa_noalloc_scratch_bytes": (SZ, []),
         "pa_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+        "pa_kv_block_bytes": (ctypes.c_int64, [I32, I32, I32, I32, I32]),
+        "pa_kv_budget_blocks": (I32, [ctypes.c_int64, I32, I32, I32, I32, I32]),
+        "pa_bm_create": (P, [I32, I32, I32]),
+        "pa_bm_destroy": (None, [P]),
+        "pa_bm_admit": (ctypes.c_int, [P, ctypes.c_int64, P, I32, I32, P, I32, P, P]),
+        "pa_bm_commit": (ctypes.c_int, [P, ctypes.c_int64, P, I32, I32]),
+        "pa_bm_release": (ctypes.c_int, [P, ctypes.c_int64]),
+        "pa_bm_slots": (ctypes.c_int, [P, ctypes.c_int64, I32, I32, P]),
+        "pa_bm_stats": (ctypes.c_int, [P, P, P, P]),
         "pa_version": (ctypes.c_int, []),
     }
     for name, (res, args) in sig.items():
@@ -263,3 +276,76 @@ def pa_splitkv_num_partitions(batch: int, num_kv_heads: int, max_blocks: int) ->
 
 def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)
+
+
+# ----------------------------------------------------------------------------- host block manager
+def pa_kv_block_bytes(num_layers: int, num_kv_heads: int, head_dim: int, block_size: int = BLOCK_SIZE,
+                      dtype_bytes: int = 2) -> int:
+    return int(library().pa_kv_block_bytes(num_layers, num_kv_heads, head_dim, block_size, dtype_bytes))
+
+
+def pa_kv_budget_blocks(budget_bytes: int, num_layers: int, num_kv_heads: int, head_dim: int,
+                        block_size: int = BLOCK_SIZE, dtype_bytes: int = 2) -> int:
+    return int(library().pa_kv_budget_blocks(int(budget_bytes), num_layers, num_kv_heads, head_dim, block_size,
+                                             dtype_bytes))
+
+
+class BlockManager:
+    """The library's host-side KV block manager (pa_bm_*): refcounted blocks, a prefix cache
+    of full blocks, full-lifetime admission.  Block tables and slot mappings come back as
+    int32 / int64 numpy arrays, ready for the attention calls."""
+
+    def __init__(self, num_blocks: int, block_size: int = BLOCK_SIZE, prefix_cache: bool = True):
+        import numpy as np
+        self._np = np
+        self.block_size = block_size
+        self._h = library().pa_bm_create(num_blocks, block_size, 1 if prefix_cache else 0)
+        if not self._h:
+            raise PagedAttnError("pa_bm_create failed")
+
+    def close(self):
+        if self._h:
+            library().pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def admit(self, request_id: int, tokens, max_new_tokens: int):
+        """(block_table, n_cached_tokens), or None when the request is rejected."""
+        np = self._np
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        cap = (len(toks) + max_new_tokens + self.block_size - 1) // self.block_size
+        table = np.empty(max(cap, 1), dtype=np.int32)
+        nb, nc = ctypes.c_int32(0), ctypes.c_int32(0)
+        rc = library().pa_bm_admit(self._h, request_id, toks.ctypes.data, len(toks), max_new_tokens,
+                                   table.ctypes.data, len(table), ctypes.byref(nb), ctypes.byref(nc))
+        if rc == PA_ERR_REJECTED:
+            return None
+        _check(rc, "pa_bm_admit")
+        return table[:nb.value].copy(), nc.value
+
+    def commit(self, request_id: int, new_tokens, computed: int):
+        np = self._np
+        toks = np.ascontiguousarray(new_tokens if new_tokens is not None else [], dtype=np.int32)
+        _check(library().pa_bm_commit(self._h, request_id, toks.ctypes.data if len(toks) else None, len(toks),
+                                      computed), "pa_bm_commit")
+
+    def release(self, request_id: int):
+        _check(library().pa_bm_release(self._h, request_id), "pa_bm_release")
+
+    def slots(self, request_id: int, start: int, n: int):
+        np = self._np
+        out = np.empty(max(n, 1), dtype=np.int64)
+        _check(library().pa_bm_slots(self._h, request_id, start, n, out.ctypes.data), "pa_bm_slots")
+        return out[:n].copy()
+
+    def stats(self):
+        """(free, cached_idle, used) block counts."""
+        f, c, u = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+        _check(library().pa_bm_stats(self._h, ctypes.byref(f), ctypes.byref(c), ctypes.byref(u)), "pa_bm_stats")
+        return f.value, c.value, u.value
+

@@ -37,7 +37,8 @@ def nvcc() -> str:
 
 
 def sources():
-    return sorted(CSRC.glob("*.cu"))
+    # CUDA translation units and the host-only C++ ones (nvcc hands .cpp to the host compiler)
+    return sorted(list(CSRC.glob("*.cu")) + list(CSRC.glob("*.cpp")))
 
 
 def _stale(out: Path, deps) -> bool:

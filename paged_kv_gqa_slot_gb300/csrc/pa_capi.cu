@@ -360,6 +360,7 @@ const char* pa_status_str(int status) {
         case PA_ERR_OUT_OF_RANGE: return "PA_ERR_OUT_OF_RANGE";
         case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
         case PA_ERR_TOO_LARGE: return "PA_ERR_TOO_LARGE";
+        case PA_ERR_REJECTED: return "PA_ERR_REJECTED";
         default: return "PA_ERR_UNKNOWN";
     }
 }

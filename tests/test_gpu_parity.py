@@ -7,6 +7,8 @@ sweeps over sequence length, group size, head dim and partition count, the degen
 cases (empty sequences, one key, more partitions than blocks), NaN leak sentinels, and
 the device status word for out-of-pool ids.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -344,3 +346,48 @@ def test_multi_query_decode_cluster_and_empty_chunk():
     g2 = GpuCase(c2)
     compare(g2.prefill(), oracle_prefill(c2), "multi-query with an empty chunk")
     check_status_clean("multi-query cluster / empty chunk")
+
+
+def test_prefix_cache_warm_hit_end_to_end():
+    """The block manager and the kernels together: a cold request's 800 prompt tokens go
+    into the pool through its slots; after it is released, a warm request with the same
+    first 768 tokens is admitted with those 48 blocks shared, appends only its own 256
+    tokens and runs the chunked prefill over the cached prefix.  The output matches the
+    oracle's prefill over the warm request's whole sequence."""
+    Hq, Hkv, D, nblk = 32, 8, 128, 160
+    gen = torch.Generator().manual_seed(6001)
+    bf = lambda *s: torch.randn(*s, generator=gen).to(torch.bfloat16)
+    bm = pa.BlockManager(nblk)
+    toks_a = torch.randint(0, 5000, (800,), generator=gen).tolist()
+    table_a, cached_a = bm.admit(1, toks_a, 0)
+    assert cached_a == 0
+    k_pool = torch.full((nblk, Hkv, 16, D), float("nan"), dtype=torch.bfloat16)
+    v_pool = k_pool.clone()
+    k_np, v_np = u16(k_pool).copy(), u16(v_pool).copy()      # the oracle's own pool
+    kd, vd = k_pool.cuda(), v_pool.cuda()
+    pool = pa.PaPool(kd, vd)
+    orc = oracle.load()
+    k_a, v_a = bf(800, Hkv, D), bf(800, Hkv, D)
+    slots_a = bm.slots(1, 0, 800)
+    pa.pa_kv_append(pool, k_a.cuda(), v_a.cuda(), torch.from_numpy(slots_a).cuda())
+    orc.kv_append(k_np, v_np, u16(k_a), u16(v_a), slots_a)
+    bm.commit(1, [], 800)
+    bm.release(1)
+
+    toks_b = toks_a[:768] + torch.randint(0, 5000, (256,), generator=gen).tolist()
+    table_b, cached_b = bm.admit(2, toks_b, 0)
+    assert cached_b == 768 and list(table_b[:48]) == list(table_a[:48])
+    k_b, v_b = bf(256, Hkv, D), bf(256, Hkv, D)
+    slots_b = bm.slots(2, 768, 256)
+    pa.pa_kv_append(pool, k_b.cuda(), v_b.cuda(), torch.from_numpy(slots_b).cuda())
+    orc.kv_append(k_np, v_np, u16(k_b), u16(v_b), slots_b)
+    q = bf(256, Hq, D)
+    bt = torch.from_numpy(table_b.astype(np.int32)).view(1, -1)
+    sl = torch.tensor([1024], dtype=torch.int32)
+    cu = torch.tensor([0, 256], dtype=torch.int32)
+    scale = 1.0 / math.sqrt(D)
+    out = pa.pa_prefill_chunked(pool, q.cuda(), cu.cuda(), bt.cuda(), sl.cuda(), scale, 256)
+    check_status_clean("warm prefix hit")
+    assert np.array_equal(u16(kd.cpu()), k_np) and np.array_equal(u16(vd.cpu()), v_np)
+    ref = orc.prefill(k_np, v_np, u16(q), cu.numpy(), bt.numpy(), sl.numpy(), scale)
+    compare(out, ref, "warm prefix hit through the block manager")
