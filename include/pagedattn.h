@@ -83,7 +83,8 @@ typedef struct {
  *   k_new, v_new   [num_tokens, num_kv_heads, head_dim] bf16, 16-byte aligned
  *   slot_mapping   [num_tokens] int64; < 0 skips the row; >= num_blocks*16 is skipped and
  *                  sets PA_DEV_OUT_OF_RANGE.  Duplicate slots are a caller error.
- * Bit-exact copy.  num_tokens == 0 is a no-op.
+ * Bit-exact copy.  num_tokens == 0 is a no-op; a call that would move 2^31 or more
+ * 16-byte chunks (num_tokens * 2 * num_kv_heads * head_dim / 8) is PA_ERR_INVALID_ARG.
  */
 int pa_kv_append(const pa_pool *pool, const void *k_new, const void *v_new, const int64_t *slot_mapping,
                  int32_t num_tokens, pa_stream_t stream);

@@ -21,30 +21,29 @@ namespace {
 __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                                         const uint4* __restrict__ k_new,
                                                         const uint4* __restrict__ v_new,
-                                                        const int64_t* __restrict__ slots, long long per_tensor,
+                                                        const int64_t* __restrict__ slots, int num_tokens,
                                                         int num_kv_heads, int chunks, long long pool_slots,
                                                         unsigned* status) {
     pdl_trigger();
     pdl_wait();
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < 2 * per_tensor; i += stride) {
-        const bool is_v = i >= per_tensor;
-        const long long j = is_v ? i - per_tensor : i;
-        const int c = static_cast<int>(j % chunks);
-        const long long th = j / chunks;
-        const int h = static_cast<int>(th % num_kv_heads);
-        const long long t = th / num_kv_heads;
+    const int row = num_kv_heads * chunks;  // 16-byte chunks of one token's K (or V) row
+    const int per_tok = 2 * row;
+    const int total = num_tokens * per_tok;  // < 2^31, checked by the launcher
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+        const int t = i / per_tok, r = i - t * per_tok;
+        const bool is_v = r >= row;
+        const int j = is_v ? r - row : r;  // h * chunks + c
+        // the source chunk does not depend on the slot: both loads are in flight together
+        const uint4 val = __ldg((is_v ? v_new : k_new) + (size_t)t * row + j);
         const int64_t slot = __ldg(slots + t);
         if (slot < 0) continue;
         if (slot >= pool_slots) {
-            if (c == 0 && h == 0 && !is_v) atomicOr(status, kDevOutOfRange);
+            if (j == 0 && !is_v) atomicOr(status, kDevOutOfRange);
             continue;
         }
-        const long long dst = (((slot / kBlockSize) * num_kv_heads + h) * kBlockSize + slot % kBlockSize) * chunks + c;
-        if (is_v)
-            v_cache[dst] = __ldg(v_new + j);
-        else
-            k_cache[dst] = __ldg(k_new + j);
+        const int h = j / chunks, c = j - h * chunks;
+        const size_t dst = (((size_t)(slot / kBlockSize) * num_kv_heads + h) * kBlockSize + slot % kBlockSize) * chunks + c;
+        (is_v ? v_cache : k_cache)[dst] = val;
     }
 }
 
@@ -53,8 +52,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
 cudaError_t launch_kv_append(const PoolView& pool, const void* k_new, const void* v_new, const int64_t* slots,
                              int num_tokens, unsigned* status, cudaStream_t stream) {
     const int chunks = pool.head_dim * 2 / 16;
-    const long long per_tensor = (long long)num_tokens * pool.num_kv_heads * chunks;
-    const long long want = (2 * per_tensor + 255) / 256;
+    const long long total = (long long)num_tokens * 2 * pool.num_kv_heads * chunks;
+    if (total >= (1LL << 31)) return cudaErrorInvalidValue;
+    const long long want = (total + 255) / 256;
     const int blocks = static_cast<int>(std::max(1LL, std::min<long long>(want, (long long)device_info().num_sms * 16)));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(blocks);
@@ -64,7 +64,7 @@ cudaError_t launch_kv_append(const PoolView& pool, const void* k_new, const void
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<uint4*>(pool.k), static_cast<uint4*>(pool.v),
-                              static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, per_tensor,
+                              static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slots, num_tokens,
                               pool.num_kv_heads, chunks, (long long)pool.num_blocks * kBlockSize, status);
 }
 

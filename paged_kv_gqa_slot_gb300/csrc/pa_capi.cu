@@ -178,6 +178,7 @@ int pa_kv_append(const pa_pool* pool, const void* k_new, const void* v_new, cons
     if (num_tokens < 0) return PA_ERR_INVALID_ARG;
     if (num_tokens == 0) return PA_OK;
     if (!k_new || !v_new || !slot_mapping || !aligned16(k_new) || !aligned16(v_new)) return PA_ERR_INVALID_ARG;
+    if ((long long)num_tokens * 2 * v.num_kv_heads * (v.head_dim / 8) >= (1LL << 31)) return PA_ERR_INVALID_ARG;
     unsigned* st = device_status_ptr();
     if (!st) return PA_ERR_CUDA;
     return from_cuda(launch_kv_append(v, k_new, v_new, slot_mapping, num_tokens, st, (cudaStream_t)stream));

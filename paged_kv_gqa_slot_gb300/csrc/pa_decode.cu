@@ -351,24 +351,37 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const float
     pdl_trigger();
     pdl_wait();
     const float* lse = ws_lse + (size_t)r * P;
+    const float4* op = reinterpret_cast<const float4*>(ws_o + (size_t)r * P * D) + lane;
+    // This warp's first partitions (p = warp + 8k) are loaded together with the lse values:
+    // the O slices do not depend on the maximum, so both round trips overlap.
+    constexpr int kPre = 4;  // covers P <= 32 in one go
+    float4 vpre[kPre];
+    float lpre[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const int p = warp + k * kCombineWarps;
+        const bool in = p < P && lane < kQuads;
+        vpre[k] = in ? __ldg(op + (size_t)p * kQuads) : make_float4(0.f, 0.f, 0.f, 0.f);
+        lpre[k] = p < P ? __ldg(lse + p) : -INFINITY;
+    }
     float M = -INFINITY;
     for (int p = lane; p < P; p += 32) M = fmaxf(M, __ldg(lse + p));
     M = warp_max(M);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
-    if (M != -INFINITY && lane < kQuads) {
-        const float4* op = reinterpret_cast<const float4*>(ws_o + (size_t)r * P * D) + lane;
-#pragma unroll 4
-        for (int p = warp; p < P; p += kCombineWarps) {
-            const float lp = __ldg(lse + p);
-            const float w = lp == -INFINITY ? 0.f : fast_exp2((lp - M) * kLog2e);
-            const float4 v = __ldg(op + (size_t)p * kQuads);  // empty partitions hold zeros
+    if (M != -INFINITY) {
+        auto add = [&](float lp, const float4& v) {
+            const float w = lp == -INFINITY ? 0.f : fast_exp2((lp - M) * kLog2e);  // empty partitions hold zeros
             den += w;
             acc.x += w * v.x;
             acc.y += w * v.y;
             acc.z += w * v.z;
             acc.w += w * v.w;
-        }
+        };
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) add(lpre[k], vpre[k]);
+        for (int p = warp + kPre * kCombineWarps; p < P; p += kCombineWarps)
+            add(__ldg(lse + p), lane < kQuads ? __ldg(op + (size_t)p * kQuads) : make_float4(0.f, 0.f, 0.f, 0.f));
     }
     if (lane < kQuads) part[warp][lane] = acc;
     if (lane == 0) dpart[warp] = den;
