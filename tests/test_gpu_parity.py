@@ -391,3 +391,53 @@ def test_prefix_cache_warm_hit_end_to_end():
     assert np.array_equal(u16(kd.cpu()), k_np) and np.array_equal(u16(vd.cpu()), v_np)
     ref = orc.prefill(k_np, v_np, u16(q), cu.numpy(), bt.numpy(), sl.numpy(), scale)
     compare(out, ref, "warm prefix hit through the block manager")
+
+
+def test_decode_large_batch_and_pool():
+    """2048 sequences (a grid dimension far past the SM count) over a 65536-block pool whose
+    block ids run to the end of the pool; decode and the split-KV path."""
+    case = W.random_case(5600, batch=2048, num_heads=8, num_kv_heads=1, head_dim=128, min_len=1, max_len=48,
+                         num_blocks=65536)
+    assert int(case.block_tables.max()) > 60000
+    g = GpuCase(case)
+    ref = oracle_decode(case)
+    compare(g.decode(), ref, "decode, 2048 sequences")
+    ws_o, ws_lse = g.splitkv(3)
+    compare(pa.pa_combine(ws_o, ws_lse), ref, "split-KV, 2048 sequences")
+    check_status_clean("large batch / pool")
+
+
+def test_prefill_whole_sequence_chunks():
+    """Chunks that are the whole sequence (no cached prefix): 1000 queries (32 query tiles,
+    16 tile pairs, 4-CTA clusters), an odd tile count (517 queries) and a single token."""
+    case = W.paged_case(name="whole_seq", seed=5601, seq_lens=[1000, 517, 1], q_lens=[1000, 517, 1],
+                        new_lens=[1000, 517, 1], num_heads=32, num_kv_heads=8, head_dim=128, num_blocks=256)
+    g = GpuCase(case)
+    compare(g.prefill(), oracle_prefill(case), "whole-sequence chunks")
+    check_status_clean("whole-sequence chunks")
+
+
+def test_prefill_group16_and_oversized_max_chunk():
+    """Group 16 on the tensor-core prefill (8 queries per 128-row tile), and a max_chunk far
+    above the longest chunk (the grid is sized for it; the extra tiles have no rows)."""
+    case = W.random_case(5602, batch=3, num_heads=64, num_kv_heads=4, head_dim=128, min_len=40, max_len=400,
+                         q_len=150, prefill=True, shared_prefix_tokens=16)
+    g = GpuCase(case)
+    ref = oracle_prefill(case)
+    compare(g.prefill(), ref, "prefill group 16")
+    out = pa.pa_prefill_chunked(g.pool, g.q, g.cu, g.bt, g.sl, case.scale, 2000)
+    compare(out, ref, "prefill with max_chunk 2000")
+    check_status_clean("group 16 / oversized max_chunk")
+
+
+def test_decode_seq_len_past_table_is_flagged():
+    """seq_len beyond max_blocks * 16 is clamped to the table and reported; the other
+    sequences are unaffected."""
+    case = W.random_case(5603, batch=3, num_heads=8, num_kv_heads=2, head_dim=128, min_len=20, max_len=60)
+    g = GpuCase(case)
+    sl = g.sl.clone()
+    sl[1] = case.block_tables.shape[1] * 16 + 5
+    out = pa.pa_decode(g.pool, g.q, g.bt, sl, case.scale)
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    ref = oracle_decode(case)
+    compare(out[[0, 2]], ref[[0, 2]], "decode beside a clamped sequence")
