@@ -508,7 +508,8 @@ def run_reference(args, ws, rank):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(mean_s * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": base_config(),
+            "config": {**base_config(), "l2": "not applicable (host CPU)",
+                       "timing": "host wall clock (time.perf_counter) around each oracle step, one thread"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": describe_sample(sample)},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
