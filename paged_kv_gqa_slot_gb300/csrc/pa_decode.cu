@@ -85,7 +85,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + Sh::data_bytes(stages));
     uint64_t* empty = full + stages;
 
-    const int split = blockIdx.x, nsplit = gridDim.x, kvh = blockIdx.y, b = blockIdx.z;
+    // The `sub` CTAs of a thread-block cluster (1 without one) share one result: a partition
+    // of split-KV, or the whole sequence of a clustered decode.  x = result * sub + rank.
+    uint32_t ncl;
+    asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(ncl));
+    const int sub = static_cast<int>(ncl);
+    const int parts = gridDim.x / sub;                      // partitions (split-KV) or 1
+    const int unit = blockIdx.x / sub, sub_rank = blockIdx.x % sub;
+    const int kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = a.group;
     pdl_wait();
@@ -109,9 +116,14 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     }
     const int R = MQ ? C * g : g;  // columns in use
     const int nb = (L + kBlockSize - 1) / kBlockSize;
-    const int per = (nb + nsplit - 1) / nsplit;
-    const int blk0 = split * per;
-    const int n = R == 0 ? 0 : max(0, min(per, nb - blk0));
+    // partition `unit` covers blocks [unit * per_u, (unit + 1) * per_u) (ceil(nb / parts) each);
+    // its sub CTAs take equal consecutive shares of them
+    const int per_u = (nb + parts - 1) / parts;
+    const int u0 = unit * per_u;
+    const int nu = max(0, min(per_u, nb - u0));
+    const int per = (nu + sub - 1) / sub;
+    const int blk0 = u0 + sub_rank * per;
+    const int n = R == 0 ? 0 : max(0, min(per, nu - sub_rank * per));
 
     if (a.k_new != nullptr && warp == 0 && nb > 0 && blk0 + n == nb && n > 0) {
         // Fused append: the CTA that reads the sequence's last block first writes the new K/V
@@ -259,11 +271,11 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     }
     __syncthreads();
 
-    if (SPLIT) {
-        // partition `split` of nsplit: normalised O_p and natural-log lse_p
+    if (SPLIT && sub == 1) {
+        // partition `unit` of parts: normalised O_p and natural-log lse_p
         for (int e = threadIdx.x; e < E; e += kThreads) {
             const int h = e / D, dd = e % D;
-            const size_t row = ((size_t)b * a.num_heads + (size_t)kvh * g + h) * nsplit + split;
+            const size_t row = ((size_t)b * a.num_heads + (size_t)kvh * g + h) * parts + unit;
             const float den = cta[16 + h];
             a.ws_o[row * D + dd] = den > 0.f ? cta[32 + e] / den : 0.f;
             if (dd == 0) a.ws_lse[row] = den > 0.f ? (cta[h] + log2f(den)) * kLn2 : -INFINITY;
@@ -276,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         const size_t tok = MQ ? (size_t)q0 + row / g : (size_t)b;
         return a.out + (tok * a.num_heads + (size_t)kvh * g + (MQ ? row % g : row)) * D + e % D;
     };
-    if (nsplit == 1) {
+    if (sub == 1) {
         for (int e = threadIdx.x; e < E; e += kThreads) {
             const float den = cta[16 + e / D];
             *out_at(e) = __float2bfloat16_rn(den > 0.f ? cta[32 + e] / den : 0.f);
@@ -288,10 +300,11 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     // (one remote load per thread), then the O slices as independent 16-byte loads.
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
-    float* wgt = part;  // [nsplit][16] merge weights, then den[16] (the warp partials are done)
+    float* wgt = part;  // [sub][16] merge weights, then den[16], max[16] (the warp partials are done)
     float* den = part + 16 * 16;
+    float* mrow = part + 16 * 16 + 16;
     const int rank = static_cast<int>(cluster.block_rank());
-    for (int t = threadIdx.x; t < nsplit * R; t += kThreads) {
+    for (int t = threadIdx.x; t < sub * R; t += kThreads) {
         const int r = t / R, h = t % R;
         const float* rc = cluster.map_shared_rank(cta, r);
         wgt[r * 16 + h] = rc[h];
@@ -301,23 +314,24 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     if (threadIdx.x < R) {
         const int h = threadIdx.x;
         float M = -INFINITY;
-        for (int r = 0; r < nsplit; ++r) M = fmaxf(M, wgt[r * 16 + h]);
+        for (int r = 0; r < sub; ++r) M = fmaxf(M, wgt[r * 16 + h]);
         float dsum = 0.f;
-        for (int r = 0; r < nsplit; ++r) {
+        for (int r = 0; r < sub; ++r) {
             const float m = wgt[r * 16 + h];
             const float w = m == -INFINITY ? 0.f : fast_exp2(m - M);
             wgt[r * 16 + h] = w;
             dsum += w * wgt[256 + 32 + r * 16 + h];
         }
         den[h] = dsum;
+        mrow[h] = M;
     }
     __syncthreads();
     const int quads = E / 4;
-    const int qper = (quads + nsplit - 1) / nsplit;
+    const int qper = (quads + sub - 1) / sub;
     for (int qd = rank * qper + threadIdx.x; qd < min(quads, (rank + 1) * qper); qd += kThreads) {
         const int e = qd * 4, h = e / D;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int r = 0; r < nsplit; ++r) {
+        for (int r = 0; r < sub; ++r) {
             const float w = wgt[r * 16 + h];
             const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(cta, r) + 32 + e);
             acc.x += w * v.x;
@@ -326,9 +340,20 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             acc.w += w * v.w;
         }
         const float inv = den[h] > 0.f ? 1.f / den[h] : 0.f;
-        __nv_bfloat16* dst = out_at(e);  // 4 consecutive d of one row (D is a multiple of 4)
-        *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-        *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        if (SPLIT) {
+            // the partition's normalised O_p slice and (once per row) its natural-log lse_p
+            const size_t row = ((size_t)b * a.num_heads + (size_t)kvh * g + h) * parts + unit;
+            float* wo = a.ws_o + row * D + e % D;
+            wo[0] = acc.x * inv;
+            wo[1] = acc.y * inv;
+            wo[2] = acc.z * inv;
+            wo[3] = acc.w * inv;
+            if (e % D == 0) a.ws_lse[row] = den[h] > 0.f ? (mrow[h] + log2f(den[h])) * kLn2 : -INFINITY;
+        } else {
+            __nv_bfloat16* dst = out_at(e);  // 4 consecutive d of one row (D is a multiple of 4)
+            *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        }
     }
     cluster.sync();  // keep this CTA's partial alive until every reader is done
 }
@@ -421,7 +446,8 @@ int stages_for(int /*ctas*/) {
 }
 
 template <int D, int NT, bool SPLIT, bool MQ = false>
-cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cudaStream_t stream) {
+// grid_x CTAs per (sequence, kv head), in thread-block clusters of `cluster` (1: none)
+cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int grid_x, int cluster, cudaStream_t stream) {
     using Sh = DecodeShape<D>;
     auto kern = decode_kernel<D, NT, SPLIT, MQ>;
     static bool configured = false;  // per instantiation; attribute setting is idempotent
@@ -453,7 +479,7 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cuda
     da.num_blocks = pool.num_blocks;
     da.group = a.num_heads / pool.num_kv_heads;
     da.scale_log2 = a.scale * kLog2e;
-    da.stages = stages_for<D>(nsplit * pool.num_kv_heads * a.batch);
+    da.stages = stages_for<D>(grid_x * pool.num_kv_heads * a.batch);
     da.k_new = static_cast<const uint4*>(a.k_new);
     da.v_new = static_cast<const uint4*>(a.v_new);
     da.slots = a.slots;
@@ -462,16 +488,16 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cuda
     da.cu_q_lens = MQ ? a.cu_q_lens : nullptr;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nsplit, pool.num_kv_heads, a.batch);
+    cfg.gridDim = dim3(grid_x, pool.num_kv_heads, a.batch);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = Sh::smem_bytes(da.stages);
     cfg.stream = stream;
     cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!SPLIT && nsplit > 1) {
+    if (cluster > 1) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = nsplit;
+        attr[1].val.clusterDim.x = cluster;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
@@ -480,13 +506,13 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int nsplit, cuda
 }
 
 template <bool SPLIT>
-cudaError_t dispatch(const PoolView& pool, const AttnArgs& a, int nsplit, cudaStream_t stream) {
+cudaError_t dispatch(const PoolView& pool, const AttnArgs& a, int grid_x, int cluster, cudaStream_t stream) {
     const int g = a.num_heads / pool.num_kv_heads;
     if (pool.head_dim == 128)
-        return g > 8 ? launch_one<128, 2, SPLIT, false>(pool, a, nsplit, stream)
-                     : launch_one<128, 1, SPLIT, false>(pool, a, nsplit, stream);
-    return g > 8 ? launch_one<64, 2, SPLIT, false>(pool, a, nsplit, stream)
-                 : launch_one<64, 1, SPLIT, false>(pool, a, nsplit, stream);
+        return g > 8 ? launch_one<128, 2, SPLIT, false>(pool, a, grid_x, cluster, stream)
+                     : launch_one<128, 1, SPLIT, false>(pool, a, grid_x, cluster, stream);
+    return g > 8 ? launch_one<64, 2, SPLIT, false>(pool, a, grid_x, cluster, stream)
+                 : launch_one<64, 1, SPLIT, false>(pool, a, grid_x, cluster, stream);
 }
 
 int max_cluster_splits() {
@@ -548,7 +574,7 @@ int splitkv_partitions_for(int batch, int num_kv_heads, int max_blocks) {
 
 cudaError_t launch_decode(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
     const int nsplit = decode_splits_for(a.batch, pool.num_kv_heads, a.max_blocks);
-    return dispatch<false>(pool, a, nsplit, stream);
+    return dispatch<false>(pool, a, nsplit, nsplit, stream);
 }
 
 bool decode_mq_supported(int group, int max_chunk) { return max_chunk >= 1 && (long long)max_chunk * group <= 16; }
@@ -558,14 +584,30 @@ cudaError_t launch_decode_mq(const PoolView& pool, const AttnArgs& a, cudaStream
     const int nsplit = decode_splits_for(a.batch, pool.num_kv_heads, a.max_blocks);
     const bool two = a.max_chunk * g > 8;
     if (pool.head_dim == 128)
-        return two ? launch_one<128, 2, false, true>(pool, a, nsplit, stream)
-                   : launch_one<128, 1, false, true>(pool, a, nsplit, stream);
-    return two ? launch_one<64, 2, false, true>(pool, a, nsplit, stream)
-               : launch_one<64, 1, false, true>(pool, a, nsplit, stream);
+        return two ? launch_one<128, 2, false, true>(pool, a, nsplit, nsplit, stream)
+                   : launch_one<128, 1, false, true>(pool, a, nsplit, nsplit, stream);
+    return two ? launch_one<64, 2, false, true>(pool, a, nsplit, nsplit, stream)
+               : launch_one<64, 1, false, true>(pool, a, nsplit, nsplit, stream);
+}
+
+// CTAs per split-KV partition: when the partitions of all (sequence, kv head) pairs leave
+// the GPU's four-per-SM wave at least half empty, each partition runs on a cluster of 2-4
+// CTAs that split its blocks and merge on chip (the partition boundaries do not change).
+int splitkv_cluster_for(int batch, int num_kv_heads, int num_partitions, int max_blocks) {
+    static const int forced = [] {
+        const char* e = std::getenv("PA_SPLITKV_CLUSTER");
+        return e ? std::atoi(e) : 0;
+    }();
+    const long long ctas = (long long)std::max(1, batch) * num_kv_heads * num_partitions;
+    int c = forced > 0 ? forced : (int)std::min<long long>(4, (4LL * device_info().num_sms) / ctas);
+    c = std::max(1, std::min(c, 8));
+    while (c > 1 && max_blocks / ((long long)num_partitions * c) < 4) --c;  // >= ~4 blocks per CTA
+    return c;
 }
 
 cudaError_t launch_decode_splitkv(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
-    return dispatch<true>(pool, a, a.num_partitions, stream);
+    const int c = splitkv_cluster_for(a.batch, pool.num_kv_heads, a.num_partitions, a.max_blocks);
+    return dispatch<true>(pool, a, a.num_partitions * c, c, stream);
 }
 
 cudaError_t launch_combine(const float* ws_o, const float* ws_lse, int batch, int num_heads, int head_dim,
