@@ -479,6 +479,21 @@ def describe_sample(s: OracleSample) -> str:
 
 
 # ----------------------------------------------------------------------------- main
+def max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks (the job is as slow as its slowest replica)."""
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value_gbs(step_kv_bytes: int, world_size: int, step_us: float) -> float:
+    """Whole-job throughput: every replica reads its own step's KV bytes in step_us."""
+    return world_size * step_kv_bytes / step_us / 1e3
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -569,12 +584,8 @@ def main(argv=None):
     if status:
         raise RuntimeError(f"device status {status:#x} after the timed steps")
 
-    mean_step_us = float(step_us.mean())
-    if ws > 1:
-        t = torch.tensor([mean_step_us], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_step_us = float(t.item())
-    value = ws * step.step_kv_bytes / mean_step_us / 1e3  # GB/s
+    mean_step_us = max_over_ranks(float(step_us.mean()), dev)
+    value = job_value_gbs(step.step_kv_bytes, ws, mean_step_us)  # GB/s
 
     # per call
     calls = {}
