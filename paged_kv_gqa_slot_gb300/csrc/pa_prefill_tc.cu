@@ -393,19 +393,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const float m_new = fmaxf(m_used, mxs);
             const bool rescale = m_new > m_used + kRescaleThreshold;  // always for the first visible key
             const int pb = j % kPBufs;
-            // P buffer pb was last read by P V(j-2); O is only touched here when it must be
-            // rescaled, and then P V(j-1) must have finished too.  A buffer's barrier cannot
-            // run two phases ahead of these waits: P V(j) needs P(j) first.
+            // P buffer pb was last read by P V(j-2), which the MMA warp issued before Q K^T(j):
+            // the commit behind s_full(j) covers every tcgen05 op issued before it, so that
+            // P V has finished.  O is touched here only when it must be rescaled, and then
+            // P V(j-1) (issued after Q K^T(j)) must have finished too; a buffer's barrier
+            // cannot run two phases ahead of that wait, since P V(j) needs P(j) first.
             const bool warp_rescale = __any_sync(0xffffffffu, rescale && m_used != -INFINITY);
-            bool wait_ok = true;
-            if (j >= kPBufs) wait_ok = mbar_wait(&bars->o_done[t][pb], ((j - kPBufs) / kPBufs) & 1);
-            if (warp_rescale && j >= 1)
-                wait_ok = mbar_wait(&bars->o_done[t][(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1) && wait_ok;
-            if (__any_sync(0xffffffffu, !wait_ok)) {
-                ok = false;
-                break;
+            if (warp_rescale && j >= 1) {
+                if (__any_sync(0xffffffffu,
+                               !mbar_wait(&bars->o_done[t][(j - 1) % kPBufs], ((j - 1) / kPBufs) & 1))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
             }
-            if (j >= 1) tc_fence_after();
             // alpha = 2^(m_old - m_new) for rows that re-base (0 while nothing was visible), else 1
             const float alpha = rescale ? fast_exp2(m_used - m_new) : 1.f;
             if (warp_rescale) {
