@@ -9,17 +9,24 @@ in HBM:
   4. pa_decode_splitkv   1 x 32768, P in 8..32 + pa_combine
   5. pa_kv_append        8 x 256 chunk tokens     (chunked prefill over a shared 768-token prefix)
   6. pa_prefill_chunked  8 x 256-token causal chunks, 32q/8kv/128
-The step is captured once as a CUDA graph and replayed, as a serving loop replays its
-decode step.  value = KV bytes the attention calls must read per step / step time (GB/s),
+The workloads are independent requests on separate pools, so the step runs each on a stream
+of its own (the prefill chain first, then the decodes), forked from and joined back into one
+stream; it is captured once as a CUDA graph with those parallel branches and replayed, as a
+serving loop replays its step.  The same calls one after another on one stream are timed too
+("step_serial_us").  value = KV bytes the attention calls must read per step / step time (GB/s),
 L2 flushed (a 512 MB buffer is read) before every timed replay, outside the timed interval.
 Each call is also captured and timed on its own and reported under "per_call".  The
 end-to-end number ("e2e") calls the public API eagerly with host buffers: every workload's
 inputs are copied up from pinned host memory on a copy stream, its calls run once they have
-arrived, and its output is copied back on a second copy stream, all inside the timed interval.  The two latency-bound decode
+arrived (each workload on its own compute stream), and its output is copied back on a second
+copy stream, all inside the timed interval.  The two latency-bound decode
 shapes (1 seq x 37 tokens, 4q/1kv/64; 1 seq x 1152 tokens, 32q/8kv/128) are reported
 under "latency" (cold and CUDA-graph-replayed).
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--serial-step]
+
+--serial-step makes the serial step the headline value (the parallel one is then reported as
+"step_parallel_us").
 
 --impl reference times the CPU fp64 oracle (the reference arm of this comparison) on a
 bounded sample of the same step.  Under torchrun (N > 1) every rank runs the full step on
@@ -246,12 +253,38 @@ class Step:
         cases = ((self.g1, self.c1), (self.g2, self.c2), (g3, c3), (g4a, c4a), (g4b, c4b), (g5, c5))
         self.step_kv_bytes = sum(c.kv_bytes() for _, c in cases if c is not None)
         self.cases = [(g, c) for g, c in cases if c is not None]
+        # parallel branches: one per workload, the longest chain (append + prefill) first
+        order = ["chunked_prefill", "batched_decode", "splitkv_4x8192", "splitkv_1x32768", "qwen3_4b_decode",
+                 "tiny_decode"]
+        self.branches = []
+        for label in order:
+            idx = [i for i, (name, _, _, _, _) in enumerate(self.calls) if call_workload(name) == label]
+            if idx:
+                self.branches.append(idx)
+        assert sorted(i for b in self.branches for i in b) == list(range(len(self.calls)))
+        self.branch_streams = [torch.cuda.Stream(device=d) for _ in self.branches]
 
     def run(self, events=None):
+        """The calls one after another on the current stream."""
         for i, (_, _, fn, _, _) in enumerate(self.calls):
             fn()
             if events is not None:
                 events[i + 1].record()
+
+    def run_parallel(self):
+        """Every workload on a stream of its own, forked from the current stream and joined
+        back into it: the workloads are independent requests on separate pools, and one
+        workload's latency-bound stretches (a kernel's start, its last wave) leave SMs and
+        HBM bandwidth that another's calls can use."""
+        main = torch.cuda.current_stream(self.dev)
+        for st in self.branch_streams:
+            st.wait_stream(main)
+        for st, idx in zip(self.branch_streams, self.branches):
+            with torch.cuda.stream(st):
+                for i in idx:
+                    self.calls[i][2]()
+        for st in self.branch_streams:
+            main.wait_stream(st)
 
     # ---- end-to-end: inputs from pinned host memory, outputs back to pinned host memory
     def e2e_setup(self):
@@ -273,11 +306,13 @@ class Step:
         self.d2h_bytes = sum(h.numel() * h.element_size() for grp in self.e2e_groups for h, _ in grp[1])
         self.s_in = torch.cuda.Stream(device=self.dev)
         self.s_out = torch.cuda.Stream(device=self.dev)
+        self.s_comp = [torch.cuda.Stream(device=self.dev) for _ in self.e2e_groups]
 
     def e2e_run(self):
         """One step as a serving loop runs it: every workload's inputs go up on one copy stream
-        as early as possible, its calls run on the compute stream once they have arrived, and its
-        output comes back on another copy stream as soon as its last call is done."""
+        as early as possible, its calls run on a compute stream of its own once they have
+        arrived, and its output comes back on another copy stream as soon as its last call is
+        done."""
         main = torch.cuda.current_stream(self.dev)
         self.s_in.wait_stream(main)
         ready = []
@@ -289,12 +324,13 @@ class Step:
                 ev.record(self.s_in)
                 ready.append(ev)
         done = []
-        for (_, _, fns), ev in zip(self.e2e_groups, ready):
-            main.wait_event(ev)
-            for fn in fns:
-                fn()
+        for (_, _, fns), ev, sc in zip(self.e2e_groups, ready, self.s_comp):
+            sc.wait_event(ev)
+            with torch.cuda.stream(sc):
+                for fn in fns:
+                    fn()
             ev2 = torch.cuda.Event()
-            ev2.record(main)
+            ev2.record(sc)
             done.append(ev2)
         with torch.cuda.stream(self.s_out):
             for (_, d2h, _), ev2 in zip(self.e2e_groups, done):
@@ -346,16 +382,22 @@ def time_graph(graph, reps, flush_buf):
     return np.array([s.elapsed_time(e) * 1e3 for s, e in ev])  # us
 
 
-def time_steps(step, steps, warmup, flush_buf, dev):
-    """The step is replayed as one CUDA graph (as a serving loop replays its decode step):
-    `steps` timed replays after `warmup` untimed ones.  Per-call times come from one graph
-    per call, timed the same way, and attribute the step's time to its calls."""
-    graph = capture_graph(step.run, dev)
+def time_steps(step, steps, warmup, flush_buf, dev, serial=False):
+    """The step is replayed as one CUDA graph (as a serving loop replays its step): `steps`
+    timed replays after `warmup` untimed ones, with the workloads as parallel branches (or
+    the calls one after another: `serial`).  The other form is timed the same way and
+    returned as `other_us`.  Per-call times come from one graph per call, timed the same
+    way."""
+    graph = capture_graph(step.run if serial else step.run_parallel, dev)
     for _ in range(warmup):
         flush_l2(flush_buf)
         graph.replay()
     torch.cuda.synchronize()
     step_us = time_graph(graph, steps, flush_buf)
+    other = capture_graph(step.run_parallel if serial else step.run, dev)
+    time_graph(other, 2, flush_buf)
+    other_us = time_graph(other, steps, flush_buf)
+    del other
     per_call = np.zeros((steps, len(step.calls)))
     for i, (_, _, fn, _, _) in enumerate(step.calls):
         g1 = capture_graph(fn, dev)
@@ -363,7 +405,7 @@ def time_steps(step, steps, warmup, flush_buf, dev):
         per_call[:, i] = time_graph(g1, steps, flush_buf)
         del g1
     del graph
-    return step_us, per_call
+    return step_us, other_us, per_call
 
 
 def time_e2e(step, steps, flush_buf):
@@ -532,10 +574,12 @@ def dist_setup():
     return ws, rank, local
 
 
-def base_config():
+def base_config(serial=False):
+    form = ("its calls one after another on one stream" if serial else
+            "its workloads (independent requests on separate pools) as parallel branches")
     return {"workload": WORKLOAD, "l2": "flushed before every timed step (512 MB buffer read)",
-            "timing": "CUDA events around each replay of the step captured as one CUDA graph; per-call "
-                      "times from one graph per call, timed the same way"}
+            "timing": f"CUDA events around each replay of the step captured as one CUDA graph, {form}; "
+                      "per-call times from one graph per call, timed the same way"}
 
 
 def run_reference(args, ws, rank):
@@ -570,6 +614,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--serial-step", action="store_true",
+                    help="headline the calls one after another on one stream instead of the parallel branches")
     ap.add_argument("--only", choices=sorted(Step.GROUPS),
                     help="time only this part of the step (for profiling); skips the extras")
     args = ap.parse_args(argv)
@@ -599,13 +645,13 @@ def main(argv=None):
     t_end = time.time() + (1.5 if extras else 0.0)
     while time.time() < t_end:
         flush_l2(flush_buf)
-        step.run()
+        (step.run if args.serial_step else step.run_parallel)()
         torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     wall0 = time.time()
-    step_us, per_call = time_steps(step, args.steps, args.warmup, flush_buf, dev)
+    step_us, other_us, per_call = time_steps(step, args.steps, args.warmup, flush_buf, dev, args.serial_step)
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
@@ -667,8 +713,10 @@ def main(argv=None):
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(mean_step_us / 1e3, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": base_config() if extras else {**base_config(), "workload": f"only {args.only}"},
+            "config": (base_config(args.serial_step) if extras else
+                       {**base_config(args.serial_step), "workload": f"only {args.only}"}),
             "step_kv_bytes": int(step.step_kv_bytes),
+            ("step_parallel_us" if args.serial_step else "step_serial_us"): round(float(other_us.mean()), 2),
             "roofline": roof, "per_call": calls, "latency": lat, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": len(step.calls) * args.steps, "clocks": clocks,
             "wall_s_timed": round(wall, 3),

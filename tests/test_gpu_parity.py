@@ -441,3 +441,21 @@ def test_decode_seq_len_past_table_is_flagged():
     assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
     ref = oracle_decode(case)
     compare(out[[0, 2]], ref[[0, 2]], "decode beside a clamped sequence")
+
+
+def test_prefill_invalid_sequence_is_skipped():
+    """A sequence whose chunk is longer than its length is skipped and flagged: its rows are
+    not written, and the sequences around it come out right."""
+    case = W.random_case(5701, batch=4, num_heads=32, num_kv_heads=8, head_dim=128, min_len=200, max_len=400,
+                         q_len=200, prefill=True)
+    g = GpuCase(case)
+    sl = g.sl.clone()
+    sl[1] = case.q_lens[1] - 1  # L < C
+    out = torch.zeros_like(g.q)
+    pa.pa_prefill_chunked(g.pool, g.q, g.cu, g.bt, sl, case.scale, max(case.q_lens), out=out)
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    ref = oracle_prefill(case)
+    cu = case.cu_q_lens.tolist()
+    keep = [i for b in (0, 2, 3) for i in range(cu[b], cu[b + 1])]
+    compare(out[keep], ref[keep], "prefill beside a skipped sequence")
+    assert not torch.any(out[cu[1]:cu[2]].float() != 0), "the skipped sequence's rows were written"
