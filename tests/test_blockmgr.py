@@ -28,6 +28,27 @@ def test_budget_arithmetic_qwen3_32b():
     assert pa.pa_kv_block_bytes(0, 8, 128) == 0 and pa.pa_kv_budget_blocks(10 ** 9, 64, 0, 128) == 0
 
 
+def test_budget_hybrid_stack():
+    """The hybrid line pages only its full-attention layers, one in four ("Qwen3.5 Dense",
+    Notes: the 8 full-attention layers of a 32-layer stack keep a paged KV cache; the other
+    24 carry a fixed-size state), so a 16-token block spans a quarter of the layers and a
+    budget holds four times as many blocks.  The attention layers' head counts are not on the
+    pages; 8 kv heads of 128 (the Qwen3 line's) stand in, and the ratio does not depend on
+    them."""
+    full, hybrid = pa.pa_kv_block_bytes(32, 8, 128), pa.pa_kv_block_bytes(8, 8, 128)
+    assert full == 4 * hybrid == 2 * 2 ** 20
+    budget = 1000 * full
+    assert pa.pa_kv_budget_blocks(budget, 32, 8, 128) == 1000
+    assert pa.pa_kv_budget_blocks(budget, 8, 8, 128) == 4000
+    # The recurrent state is reserved ahead of the KV pool (two ~147 MB states for each of
+    # the default 64 decode slots at 27B: the 18.8 GB the pages quote); the pool is sized
+    # from what is left.
+    reserve = 64 * 2 * 147 * 10 ** 6
+    assert round(reserve / 1e8) == 188
+    assert pa.pa_kv_budget_blocks(budget + reserve, 8, 8, 128) - pa.pa_kv_budget_blocks(budget, 8, 8, 128) == \
+        reserve // hybrid
+
+
 def test_full_lifetime_admission():
     bm = pa.BlockManager(10, prefix_cache=False)
     t1, c1 = bm.admit(1, range(50), 30)          # 80 tokens -> 5 blocks
