@@ -16,10 +16,15 @@ serving loop replays its step.  The same calls one after another on one stream a
 ("step_serial_us").  value = KV bytes the attention calls must read per step / step time (GB/s),
 L2 flushed (a 512 MB buffer is read) before every timed replay, outside the timed interval.
 Each call is also captured and timed on its own and reported under "per_call".  The
-end-to-end number ("e2e") calls the public API eagerly with host buffers: every workload's
-inputs are copied up from pinned host memory on a copy stream, its calls run once they have
-arrived (each workload on its own compute stream), and its output is copied back on a second
-copy stream, all inside the timed interval.  The two latency-bound decode
+end-to-end number ("e2e") runs the step through the public API with host buffers, the
+copies inside the timed interval: each workload's inputs are staged in one pinned host
+buffer; they are copied up on a copy stream, piece by piece (each decode workload whole,
+then the chunked prefill in two groups of sequences); each piece's calls run on a compute
+stream of their own once its inputs have arrived, and its output is copied back on a copy
+stream of its own as soon as it is done, while later pieces still go up or compute.  That
+e2e step is captured as one CUDA graph (copies included) and replayed, as a serving loop
+replays its step; "eager_value" issues the same step from Python call by call (host-bound).
+The e2e outputs are checked bit for bit against the step's.  The two latency-bound decode
 shapes (1 seq x 37 tokens, 4q/1kv/64; 1 seq x 1152 tokens, 32q/8kv/128) are reported
 under "latency" (cold and CUDA-graph-replayed).
 
@@ -189,12 +194,32 @@ class Step:
         d = device
 
         def up(c):
+            """A workload's pool, and its per-step inputs packed into one device buffer (views
+            at 256-byte aligned offsets, the small tables first, then the new K and V rows and
+            q) with a pinned host copy of the same layout: a serving loop stages a step's
+            inputs like this, so that they go up in few copies."""
             if c is None:
                 return None
-            g = {"k": c.k_cache.to(d), "v": c.v_cache.to(d), "q": c.q.to(d), "bt": c.block_tables.to(d),
-                 "sl": c.seq_lens.to(d), "cu": c.cu_q_lens.to(d), "k_new": c.k_new.to(d),
-                 "v_new": c.v_new.to(d), "slots": c.slot_mapping.to(d)}
+            g = {"k": c.k_cache.to(d), "v": c.v_cache.to(d)}
             g["pool"] = pa.PaPool(g["k"], g["v"])
+            ins = {"bt": c.block_tables, "sl": c.seq_lens, "cu": c.cu_q_lens, "slots": c.slot_mapping}
+            if c is self.c5:  # the prefill groups' cu_q_lens, rebased to 0, for the e2e pipeline
+                for i, (b0, b1) in enumerate(self.prefill_groups(c)):
+                    ins[f"cu{i}"] = c.cu_q_lens[b0:b1 + 1] - c.cu_q_lens[b0]
+            ins.update({"k_new": c.k_new, "v_new": c.v_new, "q": c.q})
+            layout, off = {}, 0
+            for key, t in ins.items():
+                off = (off + 255) // 256 * 256
+                layout[key] = off
+                off += t.numel() * t.element_size()
+            host = torch.empty(max(off, 1), dtype=torch.uint8).pin_memory()
+            dev = torch.empty(max(off, 1), dtype=torch.uint8, device=d)
+            for key, t in ins.items():
+                nb = t.numel() * t.element_size()
+                host[layout[key]:layout[key] + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+                g[key] = dev[layout[key]:layout[key] + nb].view(t.dtype).view(t.shape)
+            dev.copy_(host)
+            g["in_host"], g["in_dev"], g["in_layout"] = host, dev, layout
             g["out"] = torch.empty_like(g["q"])
             return g
 
@@ -287,44 +312,80 @@ class Step:
             main.wait_stream(st)
 
     # ---- end-to-end: inputs from pinned host memory, outputs back to pinned host memory
+    # groups of prefill sequences in the e2e pipeline (1, 2, 3 and 4 measured; 2 and 3 best)
+    E2E_PREFILL_GROUPS = 2
+
+    def prefill_groups(self, c):
+        """The e2e pipeline's groups of prefill sequences: [(b0, b1), ...]."""
+        n = max(1, min(self.E2E_PREFILL_GROUPS, c.batch))
+        edges = [c.batch * i // n for i in range(n + 1)]
+        return [(b0, b1) for b0, b1 in zip(edges[:-1], edges[1:]) if b1 > b0]
+
     def e2e_setup(self):
-        """Per workload: its inputs' pinned host copies and device tensors, its output's
-        pinned host buffer, and its calls (in step order)."""
-        self.e2e_groups = []
+        """The step's pieces, in upload order: each decode workload whole (its inputs in one
+        copy), then the chunked prefill in groups of sequences (the first group also brings
+        the workload's small tables; each group its rows of new K, new V and q, three
+        copies).  A piece is its host-to-device copies, its device-to-host copies and its
+        calls.  A prefill group is an append and a prefill over its own sequences (views of
+        the workload's tensors, cu_q_lens rebased to 0): the same per-sequence arithmetic as
+        the one-launch prefill, so the same bits."""
+        pa = self.pa
+        self.e2e_pieces = []
         for g, c in self.cases:
-            h2d = []
-            for key, src in (("q", c.q), ("bt", c.block_tables), ("sl", c.seq_lens), ("cu", c.cu_q_lens),
-                             ("k_new", c.k_new), ("v_new", c.v_new), ("slots", c.slot_mapping)):
-                if src.numel() == 0:
-                    continue
-                h2d.append((src.contiguous().pin_memory(), g[key]))
+            if c is self.c5:
+                continue
             d2h = [(torch.empty_like(g["out"], device="cpu").pin_memory(), g["out"])]
             fns = [fn for (name, _, fn, _, _) in self.calls if call_workload(name) == c.name]
-            self.e2e_groups.append((h2d, d2h, fns))
-        assert sum(len(f) for _, _, f in self.e2e_groups) == len(self.calls)
-        self.h2d_bytes = sum(h.numel() * h.element_size() for grp in self.e2e_groups for h, _ in grp[0])
-        self.d2h_bytes = sum(h.numel() * h.element_size() for grp in self.e2e_groups for h, _ in grp[1])
+            self.e2e_pieces.append(([(g["in_host"], g["in_dev"])], d2h, fns, c.name))
+        if self.c5 is not None:
+            g, c = self.g5, self.c5
+            assert c.k_new.shape[0] == sum(c.q_lens), "prefill workload: one appended row per chunk query"
+            cu = c.cu_q_lens.tolist()
+            lay, hb, db = g["in_layout"], g["in_host"], g["in_dev"]
+            row = c.k_new[0].numel() * 2  # bytes of one new K (or V) row
+            qrow = c.q[0].numel() * 2
+            for i, (b0, b1) in enumerate(self.prefill_groups(c)):
+                r0, r1 = cu[b0], cu[b1]
+                h2d = [(hb[lay["bt"]:lay["k_new"]], db[lay["bt"]:lay["k_new"]])] if i == 0 else []
+                for key, rb in (("k_new", row), ("v_new", row), ("q", qrow)):
+                    h2d.append((hb[lay[key] + r0 * rb:lay[key] + r1 * rb], db[lay[key] + r0 * rb:lay[key] + r1 * rb]))
+                dv = {"q": g["q"][r0:r1], "k_new": g["k_new"][r0:r1], "v_new": g["v_new"][r0:r1],
+                      "slots": g["slots"][r0:r1], "bt": g["bt"][b0:b1], "sl": g["sl"][b0:b1], "cu": g[f"cu{i}"],
+                      "out": g["out"][r0:r1]}
+                d2h = [(torch.empty_like(dv["out"], device="cpu").pin_memory(), dv["out"])]
+                mx = max(c.q_lens[b0:b1])
+                fns = [lambda dv=dv: pa.pa_kv_append(g["pool"], dv["k_new"], dv["v_new"], dv["slots"]),
+                       lambda dv=dv, mx=mx: pa.pa_prefill_chunked(g["pool"], dv["q"], dv["cu"], dv["bt"], dv["sl"],
+                                                                 c.scale, mx, dv["out"])]
+                self.e2e_pieces.append((h2d, d2h, fns, c.name))
+        self.h2d_bytes = sum(h.numel() * h.element_size() for pc in self.e2e_pieces for h, _ in pc[0])
+        self.d2h_bytes = sum(h.numel() * h.element_size() for pc in self.e2e_pieces for h, _ in pc[1])
+        # the prefill groups' calls on high-priority streams: the copies of their large output
+        # wait for them, so their CTAs take SMs ahead of the decodes' as SMs free up
+        lo, hi = torch.cuda.Stream.priority_range()
         self.s_in = torch.cuda.Stream(device=self.dev)
-        self.s_out = torch.cuda.Stream(device=self.dev)
-        self.s_comp = [torch.cuda.Stream(device=self.dev) for _ in self.e2e_groups]
+        self.s_comp = [torch.cuda.Stream(device=self.dev, priority=hi if label == "chunked_prefill" else 0)
+                       for _, _, _, label in self.e2e_pieces]
+        self.s_out = [torch.cuda.Stream(device=self.dev) for _ in self.e2e_pieces]
 
     def e2e_run(self):
-        """One step as a serving loop runs it: every workload's inputs go up on one copy stream
-        as early as possible, its calls run on a compute stream of its own once they have
+        """One step as a serving loop runs it: every piece's inputs go up on one copy stream as
+        early as possible, its calls run on a compute stream of its own once they have
         arrived, and its output comes back on another copy stream as soon as its last call is
-        done."""
+        done (one copy stream per piece, so that none waits behind another's output), while
+        later pieces are still going up or computing."""
         main = torch.cuda.current_stream(self.dev)
         self.s_in.wait_stream(main)
         ready = []
         with torch.cuda.stream(self.s_in):
-            for h2d, _, _ in self.e2e_groups:
+            for h2d, _, _, _ in self.e2e_pieces:
                 for h, dv in h2d:
                     dv.copy_(h, non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(self.s_in)
                 ready.append(ev)
         done = []
-        for (_, _, fns), ev, sc in zip(self.e2e_groups, ready, self.s_comp):
+        for (_, _, fns, _), ev, sc in zip(self.e2e_pieces, ready, self.s_comp):
             sc.wait_event(ev)
             with torch.cuda.stream(sc):
                 for fn in fns:
@@ -332,12 +393,20 @@ class Step:
             ev2 = torch.cuda.Event()
             ev2.record(sc)
             done.append(ev2)
-        with torch.cuda.stream(self.s_out):
-            for (_, d2h, _), ev2 in zip(self.e2e_groups, done):
-                self.s_out.wait_event(ev2)
+        for (_, d2h, _, _), ev2, so in zip(self.e2e_pieces, done, self.s_out):
+            so.wait_event(ev2)
+            with torch.cuda.stream(so):
                 for h, dv in d2h:
                     h.copy_(dv, non_blocking=True)
-        main.wait_stream(self.s_out)
+            main.wait_stream(so)
+
+    def e2e_outputs(self):
+        """Host copies of every workload's output after an e2e step: {workload: tensor}, the
+        prefill groups joined in sequence order."""
+        outs = {}
+        for _, d2h, _, label in self.e2e_pieces:
+            outs.setdefault(label, []).extend(h for h, _ in d2h)
+        return {k: torch.cat(v) for k, v in outs.items()}
 
 
 def call_workload(name: str) -> str:
@@ -409,12 +478,16 @@ def time_steps(step, steps, warmup, flush_buf, dev, serial=False):
 
 
 def time_e2e(step, steps, flush_buf):
+    """End-to-end step time (us): the e2e step (uploads, calls, downloads) replayed as one
+    CUDA graph, as a serving loop replays its step with inputs staged in fixed pinned
+    buffers; the copies run on every replay.  Also the same step issued eagerly from Python
+    (host-bound: every copy and call is a few microseconds of host work)."""
     step.e2e_setup()
     torch.cuda.synchronize()
-    ts = []
     for _ in range(2):  # warm the copies
         step.e2e_run()
     torch.cuda.synchronize()
+    eager = []
     for _ in range(steps):
         flush_l2(flush_buf)
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -422,8 +495,21 @@ def time_e2e(step, steps, flush_buf):
         step.e2e_run()
         e.record()
         e.synchronize()
-        ts.append(s.elapsed_time(e) * 1e3)
-    return float(np.mean(ts))
+        eager.append(s.elapsed_time(e) * 1e3)
+    graph = capture_graph(step.e2e_run, step.dev)
+    time_graph(graph, 2, flush_buf)
+    replay = time_graph(graph, steps, flush_buf)
+    torch.cuda.synchronize()
+    # The pipelined pieces must give the very bits of the step's calls: run those (one
+    # prefill launch) on the same inputs and compare every workload's output.
+    got = {k: v.clone() for k, v in step.e2e_outputs().items()}
+    del graph
+    step.run()
+    torch.cuda.synchronize()
+    for g, c in step.cases:
+        if not torch.equal(got[c.name], g["out"].cpu()):
+            raise RuntimeError(f"e2e output of {c.name} differs from the step's")
+    return float(np.mean(replay)), float(np.mean(eager))
 
 
 def latency_configs(flush_buf):
@@ -694,9 +780,11 @@ def main(argv=None):
     # end to end through the public API with host buffers
     e2e, lat = None, {}
     if extras:
-        e2e_us = time_e2e(step, max(5, min(args.steps, 20)), flush_buf)
+        e2e_us, eager_us = time_e2e(step, max(5, min(args.steps, 20)), flush_buf)
         e2e = {"value": round(step.step_kv_bytes / e2e_us / 1e3, 1), "unit": "GB/s",
-               "h2d_bytes_per_step": int(step.h2d_bytes), "d2h_bytes_per_step": int(step.d2h_bytes)}
+               "h2d_bytes_per_step": int(step.h2d_bytes), "d2h_bytes_per_step": int(step.d2h_bytes),
+               "us_per_step": round(e2e_us, 1), "timing": "the e2e step replayed as one CUDA graph",
+               "eager_value": round(step.step_kv_bytes / eager_us / 1e3, 1)}
         lat = latency_configs(flush_buf) if rank == 0 else {}
 
     cpu = None
