@@ -17,6 +17,7 @@
 //   * pa_decode_splitkv writes each partition's normalised O_p and lse_p to the caller's
 //     workspace for pa_combine.
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 
 #include <cooperative_groups.h>
@@ -450,8 +451,8 @@ template <int D, int NT, bool SPLIT, bool MQ = false>
 cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int grid_x, int cluster, cudaStream_t stream) {
     using Sh = DecodeShape<D>;
     auto kern = decode_kernel<D, NT, SPLIT, MQ>;
-    static bool configured = false;  // per instantiation; attribute setting is idempotent
-    if (!configured) {
+    static OncePerDevice configured;  // per instantiation
+    cudaError_t se = configured.run([&] {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Sh::smem_bytes(Sh::kMaxStages));
         if (e != cudaSuccess) return e;
@@ -459,12 +460,10 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int grid_x, int 
         // depths do not reconfigure the SMs between kernels
         e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
-        if (!SPLIT) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-            if (e != cudaSuccess) return e;
-        }
-        configured = true;
-    }
+        if (!SPLIT) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return e;
+    });
+    if (se != cudaSuccess) return se;
     DecodeArgs da;
     da.q = static_cast<const __nv_bfloat16*>(a.q);
     da.block_tables = a.block_tables;
@@ -516,9 +515,12 @@ cudaError_t dispatch(const PoolView& pool, const AttnArgs& a, int grid_x, int cl
 }
 
 int max_cluster_splits() {
-    // Largest cluster the decode kernel can run with (16 needs the non-portable opt-in).
-    static int cached = 0;
-    if (cached) return cached;
+    // Largest cluster the decode kernel can run with on the current device (16 needs the
+    // non-portable opt-in), asked once per device.
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 8;
+    if (const int c = cached[dev].load(std::memory_order_relaxed)) return c;
     int best = 8;
     auto kern = decode_kernel<128, 1, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
@@ -539,8 +541,8 @@ int max_cluster_splits() {
         if (cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg) == cudaSuccess && nclusters > 0) best = 16;
     }
     cudaGetLastError();
-    cached = best;
-    return cached;
+    cached[dev].store(best, std::memory_order_relaxed);
+    return best;
 }
 
 }  // namespace

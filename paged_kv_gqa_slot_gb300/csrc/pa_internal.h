@@ -3,8 +3,10 @@
 #pragma once
 
 #include <cuda.h>
+#include <atomic>
 #include <cstdlib>
 #include <cuda_runtime.h>
+#include <mutex>
 #include <stdint.h>
 
 namespace pa {
@@ -59,6 +61,30 @@ struct AttnArgs {
 
 const DeviceInfo& device_info();
 unsigned* device_status_ptr();
+
+// One-time set-up of a kernel (function attributes, occupancy queries) on each device:
+// function attributes are per device, and library calls may come from several host threads
+// at once.  `run` calls `setup` on the current device's first use, under a lock, and
+// remembers success; a failed set-up is retried by the next call.
+class OncePerDevice {
+  public:
+    template <typename F>
+    cudaError_t run(F&& setup) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevices) return cudaErrorInvalidDevice;
+        if (done_[dev].load(std::memory_order_acquire)) return cudaSuccess;
+        std::lock_guard<std::mutex> lk(mu_);
+        if (done_[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+        const cudaError_t e = setup();
+        if (e == cudaSuccess) done_[dev].store(true, std::memory_order_release);
+        return e;
+    }
+
+  private:
+    static constexpr int kDevices = 64;
+    std::mutex mu_;
+    std::atomic<bool> done_[kDevices] = {};
+};
 
 // Launch attribute that lets a kernel overlap its launch with the previous kernel's tail
 // (the kernel itself waits for that kernel before touching memory).  Off unless PA_PDL=1:

@@ -157,7 +157,9 @@ template <int D>
 cudaError_t launch_mma(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
     using Sh = PrefillShape<D>;
     auto kern = prefill_mma_kernel<D>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemBytes);
+    static OncePerDevice configured;
+    cudaError_t e = configured.run(
+        [&] { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kSmemBytes); });
     if (e != cudaSuccess) return e;
     PrefillArgs pa_;
     pa_.q = static_cast<const __nv_bfloat16*>(a.q);

@@ -527,12 +527,10 @@ bool prefill_tc_supported(int head_dim, int group) {
 }
 
 cudaError_t launch_prefill_tc(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
+    static OncePerDevice configured;
+    const cudaError_t e = configured.run(
+        [] { return cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
+    if (e != cudaSuccess) return e;
     TcArgs t;
     t.q = static_cast<const __nv_bfloat16*>(a.q);
     t.block_tables = a.block_tables;

@@ -459,3 +459,64 @@ def test_prefill_invalid_sequence_is_skipped():
     keep = [i for b in (0, 2, 3) for i in range(cu[b], cu[b + 1])]
     compare(out[keep], ref[keep], "prefill beside a skipped sequence")
     assert not torch.any(out[cu[1]:cu[2]].float() != 0), "the skipped sequence's rows were written"
+
+
+_CONCURRENT_FIRST_CALLS = r'''
+import sys, threading
+import numpy as np, torch
+sys.path[:0] = [sys.argv[1], sys.argv[1] + "/tests"]
+import paged_kv_gqa_slot_gb300 as pa
+import workloads as W
+from parity import GpuCase, compare, oracle_decode, oracle_prefill, oracle_pool
+import oracle
+cases = {
+    "decode": W.random_case(5801, batch=6, num_heads=32, num_kv_heads=8, head_dim=128, min_len=30, max_len=500),
+    "decode64": W.random_case(5802, batch=3, num_heads=8, num_kv_heads=2, head_dim=64, min_len=30, max_len=300),
+    "split": W.random_case(5803, batch=2, num_heads=64, num_kv_heads=8, head_dim=128, min_len=300, max_len=900),
+    "prefill": W.random_case(5804, batch=3, num_heads=32, num_kv_heads=8, head_dim=128, min_len=100, max_len=400,
+                             q_len=150, prefill=True),
+}
+gpu = {k: GpuCase(c) for k, c in cases.items()}
+torch.cuda.synchronize()
+outs, errors = {}, []
+barrier = threading.Barrier(len(cases))
+def work(name):
+    try:
+        g, c = gpu[name], cases[name]
+        st = torch.cuda.Stream()
+        barrier.wait()
+        with torch.cuda.stream(st):
+            if name == "split":
+                outs[name] = pa.pa_combine(*g.splitkv(5))
+            elif name == "prefill":
+                outs[name] = g.prefill()
+            else:
+                outs[name] = g.decode()
+        st.synchronize()
+    except Exception as e:  # reported by the main thread
+        errors.append(f"{name}: {e!r}")
+ts = [threading.Thread(target=work, args=(n,)) for n in cases]
+for t in ts: t.start()
+for t in ts: t.join()
+assert not errors, errors
+assert pa.pa_device_status(clear=True) == 0
+for name, c in cases.items():
+    ref = oracle_prefill(c) if name == "prefill" else oracle_decode(c)
+    compare(outs[name], ref, f"concurrent first call: {name}")
+print("ok")
+'''
+
+
+def test_concurrent_first_calls_from_threads(tmp_path):
+    """The library's first calls in a process, from four host threads at once on their own
+    streams (decode d128 and d64, split-KV with its merge, the tensor-core prefill): every
+    kernel's one-time set-up runs under contention, and every result must still match the
+    oracle."""
+    import subprocess
+    import sys
+    from pathlib import Path
+    script = tmp_path / "pa_threaded_first_calls.py"
+    script.write_text(_CONCURRENT_FIRST_CALLS)
+    root = str(Path(__file__).resolve().parents[1])
+    r = subprocess.run([sys.executable, str(script), root], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
