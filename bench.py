@@ -46,6 +46,7 @@ import math
 import os
 import re
 import subprocess
+import tempfile
 import sys
 import time
 from pathlib import Path
@@ -117,8 +118,7 @@ class ClockSampler:
 
     def start(self):
         try:
-            self.out = open(ROOT / "gpurun_out" / f".clocks_{os.getpid()}.csv", "w") if (ROOT / "gpurun_out").exists() \
-                else open(f"/tmp/.clocks_{os.getpid()}.csv", "w")
+            self.out = tempfile.NamedTemporaryFile(mode="w", prefix="pa_clocks_", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
