@@ -500,12 +500,23 @@ def time_e2e(step, steps, flush_buf):
     time_graph(graph, 2, flush_buf)
     replay = time_graph(graph, steps, flush_buf)
     torch.cuda.synchronize()
-    # The pipelined pieces must give the very bits of the step's calls: run those (one
-    # prefill launch) on the same inputs and compare every workload's output.
+    # The pipelined pieces must give the very bits of the step's calls.  Poison every output
+    # first (so that a row the pieces fail to write cannot pass on an earlier step's value),
+    # replay the e2e step once, then run the step's calls (one prefill launch) on the same
+    # inputs and compare every workload's output; the device status must stay clean.
+    import paged_kv_gqa_slot_gb300 as pa
+    pa.pa_device_status(clear=True)
+    for g, _ in step.cases:
+        g["out"].fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
     got = {k: v.clone() for k, v in step.e2e_outputs().items()}
     del graph
     step.run()
     torch.cuda.synchronize()
+    status = pa.pa_device_status(clear=True)
+    if status:
+        raise RuntimeError(f"device status {status:#x} after the e2e step")
     for g, c in step.cases:
         if not torch.equal(got[c.name], g["out"].cpu()):
             raise RuntimeError(f"e2e output of {c.name} differs from the step's")
