@@ -33,13 +33,16 @@ struct KvTile {
 // `stages` slots.  Called by a whole warp; returns false if a wait timed out.  On return
 // every copy it issued has landed (or the wait for it timed out), so the caller may exit.
 template <int D>
+// `first`, when `has_first`, is this lane's entry bt[lane] loaded earlier by the caller (valid
+// for lane < n), so that the first copies need not wait for that load.
 __device__ __forceinline__ bool produce_kv_blocks(uint8_t* ring, int stages, uint64_t* full, uint64_t* empty,
                                                   const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                                   const int32_t* bt, int n, int num_blocks, int num_kv_heads,
-                                                  int kvh, unsigned* status, uint64_t policy) {
+                                                  int kvh, unsigned* status, uint64_t policy, int first = 0,
+                                                  bool has_first = false) {
     using T = KvTile<D>;
     const int lane = threadIdx.x & 31;
-    int next = (lane < n) ? __ldg(bt + lane) : 0;
+    int next = (lane < n) ? (has_first ? first : __ldg(bt + lane)) : 0;
     bool ok = true;
     int issued = 0;
     for (int c0 = 0; c0 < n && ok; c0 += 32) {

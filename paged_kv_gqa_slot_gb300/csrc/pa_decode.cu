@@ -97,6 +97,13 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = a.group;
     pdl_wait();
+    // A CTA that alone covers its sequence (no partitions, no cluster) starts at block 0: its
+    // producer loads the first 32 table entries now, in parallel with seq_lens, instead of
+    // after it, which takes one dependent memory round trip off the first copy.
+    const bool whole = parts == 1 && sub == 1;
+    int first_entry = 0;
+    if (whole && warp == kConsumerWarps && lane < a.max_blocks)
+        first_entry = __ldg(a.block_tables + (size_t)b * a.max_blocks + lane);
 
     int L = a.seq_lens[b];
     if (L < 0 || L > a.max_blocks * kBlockSize) {
@@ -175,8 +182,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             prefetch_tensormap(&tm_v);
         }
         produce_kv_blocks<D>(smem, stages, full, empty, &tm_k, &tm_v,
-                                          a.block_tables + (size_t)b * a.max_blocks + blk0, n, a.num_blocks,
-                                          a.num_kv_heads, kvh, a.status, l2_evict_first_policy());
+                             a.block_tables + (size_t)b * a.max_blocks + blk0, n, a.num_blocks, a.num_kv_heads, kvh,
+                             a.status, l2_evict_first_policy(), first_entry, whole && blk0 == 0);
     } else {
         uint32_t qb[NT][D / 16][2];
         int colpos[NT][2];  // MQ: causal limit of this thread's two columns per n-tile
