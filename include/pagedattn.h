@@ -26,7 +26,9 @@
  * Layouts (all row-major, contiguous):
  *   pool K, V      [num_blocks, num_kv_heads, 16, head_dim]   bf16, 16-byte aligned
  *   slot           block_id * 16 + offset_in_block
- *   block_tables   [batch, max_blocks] int32; entries past ceil(seq_len / 16) are never read
+ *   block_tables   [batch, max_blocks] int32; entries past ceil(seq_len / 16) never affect
+ *                  a result (a decode may load the first min(32, max_blocks) entries of a row
+ *                  before it knows seq_len, and ignores those it does not need)
  *   seq_lens       [batch] int32, tokens in the sequence including any appended this step
  *   q, out         decode [batch, num_heads, head_dim]; prefill [sum of chunk lengths,
  *                  num_heads, head_dim]; bf16, 16-byte aligned
@@ -190,7 +192,9 @@ int pa_device_status(uint32_t *flags, int32_t clear, pa_stream_t stream);
  *   process exits.  A request whose workspace (pa_splitkv_workspace_bytes) exceeds it
  *   returns PA_ERR_TOO_LARGE before any launch.
  *   The first call on a device looks up the array's device address (one-time set-up on that
- *   device); make that first call before capturing any stream into a CUDA graph.
+ *   device); make that first call before capturing any stream into a CUDA graph.  The address
+ *   is kept for the life of the process: after cudaDeviceReset on a device, do not call this
+ *   entry point on that device again (the library's module, and the array, may have moved).
  *   Every call uses the same array, so calls that may run at the same time on the GPU
  *   (different streams, or different host threads) race and must be serialised by the
  *   caller.  Nothing needs clearing between calls: each call overwrites every slot it reads.

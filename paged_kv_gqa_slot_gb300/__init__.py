@@ -135,6 +135,30 @@ def _dev(t: torch.Tensor, dtype, name: str) -> int:
     return t.data_ptr()
 
 
+def _tables(block_tables: torch.Tensor, seq_lens: torch.Tensor, batch: int) -> None:
+    """The kernels read block_tables[b] and seq_lens[b] for every b < batch."""
+    if block_tables.dim() != 2 or block_tables.shape[0] != batch or seq_lens.numel() != batch:
+        raise ValueError(f"block_tables [batch, max_blocks] and seq_lens [batch] must match batch {batch}, got "
+                         f"{tuple(block_tables.shape)} and {tuple(seq_lens.shape)}")
+
+
+def _rows(k_new: torch.Tensor, v_new: torch.Tensor, pool: "PaPool", n: int) -> None:
+    """The append kernels read n rows of [num_kv_heads, head_dim] from k_new and v_new."""
+    shape = (n, pool.num_kv_heads, pool.head_dim)
+    if tuple(k_new.shape) != shape or tuple(v_new.shape) != shape:
+        raise ValueError(f"k_new / v_new: need shape {shape}, got {tuple(k_new.shape)} / {tuple(v_new.shape)}")
+
+
+def _out(out: Optional[torch.Tensor], shape, like: torch.Tensor) -> torch.Tensor:
+    """The caller's output tensor, checked to be exactly `shape` (the kernels write all of it),
+    or a new one."""
+    if out is None:
+        return torch.empty(tuple(shape), dtype=torch.bfloat16, device=like.device)
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out: need shape {tuple(shape)}, got {tuple(out.shape)}")
+    return out
+
+
 class PaPool:
     """The paged KV pool: k_cache, v_cache = [num_blocks, num_kv_heads, 16, head_dim] bf16 on the GPU."""
 
@@ -159,6 +183,7 @@ class PaPool:
 def pa_kv_append(pool: PaPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                  stream=None) -> None:
     T = int(slot_mapping.numel())
+    _rows(k_new, v_new, pool, T)
     rc = library().pa_kv_append(pool.ref, _dev(k_new, torch.bfloat16, "k_new") if T else None,
                                 _dev(v_new, torch.bfloat16, "v_new") if T else None,
                                 _dev(slot_mapping, torch.int64, "slot_mapping") if T else None, T, _stream(stream))
@@ -168,7 +193,8 @@ def pa_kv_append(pool: PaPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_ma
 def pa_decode(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     B, Hq, _ = q.shape
-    out = torch.empty_like(q) if out is None else out
+    _tables(block_tables, seq_lens, B)
+    out = _out(out, q.shape, q)
     rc = library().pa_decode(pool.ref, _dev(q, torch.bfloat16, "q"), _dev(block_tables, torch.int32, "block_tables"),
                              block_tables.shape[1], _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale),
                              _dev(out, torch.bfloat16, "out"), _stream(stream))
@@ -181,7 +207,11 @@ def pa_append_decode(pool: PaPool, k_new: torch.Tensor, v_new: torch.Tensor, slo
                      out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """pa_kv_append of one new row per sequence followed by pa_decode, in one launch."""
     B, Hq, _ = q.shape
-    out = torch.empty_like(q) if out is None else out
+    _tables(block_tables, seq_lens, B)
+    _rows(k_new, v_new, pool, B)
+    if slot_mapping.numel() != B:
+        raise ValueError(f"slot_mapping: need {B} entries, got {slot_mapping.numel()}")
+    out = _out(out, q.shape, q)
     rc = library().pa_append_decode(pool.ref, _dev(k_new, torch.bfloat16, "k_new"), _dev(v_new, torch.bfloat16, "v_new"),
                                     _dev(slot_mapping, torch.int64, "slot_mapping"), _dev(q, torch.bfloat16, "q"),
                                     _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
@@ -199,11 +229,15 @@ def pa_decode_splitkv(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor,
                       scale: float, num_partitions: int, ws_o: Optional[torch.Tensor] = None,
                       ws_lse: Optional[torch.Tensor] = None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     B, Hq, D = q.shape
+    _tables(block_tables, seq_lens, B)
     P = int(num_partitions)
     if ws_o is None:
         ws_o = torch.empty((B, Hq, P, D), dtype=torch.float32, device=q.device)
     if ws_lse is None:
         ws_lse = torch.empty((B, Hq, P), dtype=torch.float32, device=q.device)
+    if tuple(ws_o.shape) != (B, Hq, P, D) or tuple(ws_lse.shape) != (B, Hq, P):
+        raise ValueError(f"ws_o / ws_lse: need shapes {(B, Hq, P, D)} / {(B, Hq, P)}, "
+                         f"got {tuple(ws_o.shape)} / {tuple(ws_lse.shape)}")
     rc = library().pa_decode_splitkv(pool.ref, _dev(q, torch.bfloat16, "q"),
                                      _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
                                      _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale), P,
@@ -220,7 +254,8 @@ def pa_decode_splitkv_noalloc(pool: PaPool, q: torch.Tensor, block_tables: torch
     device memory (see include/pagedattn.h).  Pass a preallocated `out` to allocate nothing
     at all; its partition results live in a static array inside the library."""
     B, Hq, _ = q.shape
-    out = torch.empty_like(q) if out is None else out
+    _tables(block_tables, seq_lens, B)
+    out = _out(out, q.shape, q)
     rc = library().pa_decode_splitkv_noalloc(pool.ref, _dev(q, torch.bfloat16, "q"),
                                              _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
                                              _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale),
@@ -236,7 +271,9 @@ def pa_noalloc_scratch_bytes() -> int:
 def pa_combine(ws_o: torch.Tensor, ws_lse: torch.Tensor, out: Optional[torch.Tensor] = None,
                stream=None) -> torch.Tensor:
     B, Hq, P, D = ws_o.shape
-    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=ws_o.device) if out is None else out
+    if tuple(ws_lse.shape) != (B, Hq, P):
+        raise ValueError(f"ws_lse: need shape {(B, Hq, P)}, got {tuple(ws_lse.shape)}")
+    out = _out(out, (B, Hq, D), ws_o)
     rc = library().pa_combine(_dev(ws_o, torch.float32, "ws_o"), _dev(ws_lse, torch.float32, "ws_lse"), B, Hq, D, P,
                               _dev(out, torch.bfloat16, "out"), _stream(stream))
     _check(rc, "pa_combine")
@@ -248,7 +285,10 @@ def pa_prefill_chunked(pool: PaPool, q: torch.Tensor, cu_q_lens: torch.Tensor, b
                        stream=None) -> torch.Tensor:
     _, Hq, _ = q.shape
     B = int(seq_lens.numel())
-    out = torch.empty_like(q) if out is None else out
+    _tables(block_tables, seq_lens, B)
+    if cu_q_lens.numel() != B + 1:
+        raise ValueError(f"cu_q_lens: need {B + 1} entries, got {cu_q_lens.numel()}")
+    out = _out(out, q.shape, q)
     rc = library().pa_prefill_chunked(pool.ref, _dev(q, torch.bfloat16, "q"), _dev(cu_q_lens, torch.int32, "cu_q_lens"),
                                       _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
                                       _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, int(max_chunk), float(scale),

@@ -88,14 +88,13 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---------------------------------------------------------------- TMA
-// 2-D tiled load multicast to the CTAs of `mask` in this cluster: the box lands at the same
-// shared-memory offset in each of them and completes on their mbarriers at `bar`'s offset.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
-                                               uint16_t mask, uint64_t policy) {
+// 2-D tiled load into this CTA's shared memory, completing on its mbarrier `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask), "l"(policy)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
@@ -187,9 +186,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 // tcgen05.mma / tcgen05.commit issued warp-wide: the whole warp executes them (so their
 // operands stay warp-uniform) and one elected lane issues.  Every lane of the warp must
-// reach them together.  A commit arrives once on the mbarrier (on `bar`'s offset in every
-// CTA of `mask` for the multicast form) when every tcgen05 op this thread issued before it
-// has finished.  MMA: D[tmem] (+)= A * B, kind::f16 (bf16 in, fp32 accumulate); A from a
+// reach them together.  A commit arrives once on the mbarrier when every tcgen05 op this
+// thread issued before it has finished.  MMA: D[tmem] (+)= A * B, kind::f16 (bf16 in, fp32 accumulate); A from a
 // shared-memory descriptor, or from tensor memory (_ts: row i in lane i, two bf16 of K per
 // 32-bit column).
 __device__ __forceinline__ void tc_mma_ew(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -214,15 +212,6 @@ __device__ __forceinline__ void tc_commit_ew(uint64_t* bar) {
         "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar))
         : "memory");
 }
-__device__ __forceinline__ void tc_commit_mc_ew(uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
 // mbar_wait by every lane of a warp, with one verdict for all (false if any lane gave up).
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity));

@@ -26,7 +26,8 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  In host code the array's
 // name is only a host-side stand-in, so the real address is looked up once per device
-// (with that device current) and cached.
+// (with that device current) and cached for the life of the process; a cudaDeviceReset
+// could move the module, which is why the header rules out calls after one.
 void* scratch_on_current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;

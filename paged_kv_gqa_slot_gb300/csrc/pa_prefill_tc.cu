@@ -28,12 +28,10 @@
 // have run; 4 slots cover the L2 round trip of the next tiles.  P is double-buffered per
 // tile, so the softmax of key tile j+1 waits for P V of tile j-1 only (long finished),
 // unless O must be rescaled.
-// The c CTAs that hold consecutive tile pairs of one (sequence, kv head) form a
-// thread-block cluster and read the same K/V: each issues 1/c of every stage's TMA boxes
-// with multicast to all members, and every member's MMA thread releases a stage to all of
-// them (multicast commit), so a stage refills once the whole cluster is done with it.
-// Members walk the union of their key tiles (a tile some other member needs is received
-// and released without compute).
+// Every CTA loads its own K/V boxes into its own shared memory.  The CTAs of one
+// (sequence, kv head) -- and, with a shared prefix, of every sequence that shares it --
+// read the same pool blocks; the copies after the first come from L2, which the loads ask
+// to keep them (evict-last policy).
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
@@ -111,10 +109,6 @@ __device__ __forceinline__ int pair_key_count(int p, int T, int tpt, int C, int 
     return max(tile_key_count(t0, tpt, C, L), tile_key_count(t1, tpt, C, L));
 }
 
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
                                                                  const __grid_constant__ TcArgs a) {
@@ -122,11 +116,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint32_t crank, cnum;
-    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
-    asm("mov.u32 %0, %%cluster_nctarank;" : "=r"(cnum));
-    const int rank = static_cast<int>(crank), csize = static_cast<int>(cnum);
-    const uint16_t all_mask = static_cast<uint16_t>((1u << csize) - 1u);
     const int p = blockIdx.x;  // tile pair
     const int kvh = blockIdx.y, b = blockIdx.z;
     pdl_wait();
@@ -134,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int q0 = a.cu_q_lens[b];
     const int C = a.cu_q_lens[b + 1] - q0;
     const int L = a.seq_lens[b];
-    if (C < 0 || L < C || L > a.max_blocks * kBlockSize) {  // the same for the whole cluster
+    if (C < 0 || L < C || L > a.max_blocks * kBlockSize) {
         if (threadIdx.x == 0 && p == 0 && kvh == 0) atomicOr(a.status, kDevOutOfRange);
         return;
     }
@@ -143,19 +132,18 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     pair_tiles(p, T, mtile[0], mtile[1]);
 #pragma unroll
     for (int t = 0; t < kTiles; ++t) ntiles[t] = (tile_key_count(mtile[t], tpt, C, L) + kKeys - 1) / kKeys;
-    int kmax_cl = 0;  // keys any member of the cluster needs
-    for (int r = 0; r < csize; ++r) kmax_cl = max(kmax_cl, pair_key_count(p + r - rank, T, tpt, C, L));
-    const int ntiles_cl = (kmax_cl + kKeys - 1) / kKeys;
-    const int nblk = (kmax_cl + kBlockSize - 1) / kBlockSize;  // pool blocks read
+    const int kmax = pair_key_count(p, T, tpt, C, L);             // keys either tile needs
+    const int ntiles_cta = (kmax + kKeys - 1) / kKeys;             // key tiles loaded
+    const int nblk = (kmax + kBlockSize - 1) / kBlockSize;         // pool blocks read
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
-            mbar_init(&bars->k_empty[s], csize);  // one release from every member
+            mbar_init(&bars->k_empty[s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars->v_full[s], 1);
-            mbar_init(&bars->v_empty[s], csize);
+            mbar_init(&bars->v_empty[s], 1);
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(&bars->q_full[t], 128);
@@ -175,15 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     tc_fence_before();
     __syncthreads();
-    // every member's barriers exist before any multicast box or release can reach them
-    cluster_sync_all();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == kKLoadWarp || warp == kVLoadWarp) {
         // ------------------------------------------------------------ TMA producers (K, V)
-        // Of the 8 boxes of a stage (4 blocks x 2 column halves) this member issues those with
-        // index % csize == rank, multicast to the whole cluster.
+        // The 8 boxes of a stage (4 blocks x 2 column halves) go out from lanes 0-7, one each.
         const bool is_k = warp == kKLoadWarp;
         const CUtensorMap* map = is_k ? &tm_k : &tm_v;
         uint64_t* full = is_k ? bars->k_full : bars->v_full;
@@ -198,11 +183,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         int c0 = 0;
         int cur = lane < nblk ? __ldg(bt + lane) : 0;
         int nxt = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
-        const bool my_box = lane < 8 && (lane % csize) == rank;
+        const bool my_box = lane < 8;
         const int box_t = lane >> 1, box_h = lane & 1;
         bool ok = true;
         int issued = 0;
-        for (int j = 0; j < ntiles_cl && ok; ++j) {
+        for (int j = 0; j < ntiles_cta && ok; ++j) {
             // pool row of block 4j + box_t (for the issuing lanes)
             if (4 * j >= c0 + 32) {
                 c0 += 32;
@@ -222,19 +207,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
             if (ok) {
                 if (my_box)
-                    tma_load_2d_mc(ring + s * kTileBytes + box_h * kHalf + box_t * 2048, map, box_h * 64, row, &full[s],
-                                   all_mask, pol);
+                    tma_load_2d(ring + s * kTileBytes + box_h * kHalf + box_t * 2048, map, box_h * 64, row, &full[s],
+                                pol);
                 ++issued;
             }
         }
         if (lane == 0) {
-            // Before the CTA may leave: every stage armed here has been filled (by every
-            // member's boxes), and every member has released it (so no release can still be
-            // on its way to this CTA's barriers).
-            for (int j = max(0, issued - kStages); j < issued; ++j) {
+            // Before the CTA may leave: every box issued here has landed.
+            for (int j = max(0, issued - kStages); j < issued; ++j)
                 if (!mbar_wait(&full[j % kStages], (j / kStages) & 1)) ok = false;
-                if (!mbar_wait(&empty[j % kStages], (j / kStages) & 1)) ok = false;
-            }
             if (!ok) atomicOr(a.status, kDevTimeout);
         }
     } else if (warp == kMmaWarp) {
@@ -256,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         for (int t = 0; t < kTiles; ++t)
             if (ok && ntiles[t] > 0) ok = mbar_wait_warp(&bars->q_full[t], 0);
         int ks_ = 0, kph = 0, vs_ = 0, vph = 0;  // ring slot and phase of K(j) and V(j-1)
-        for (int j = 0; j <= ntiles_cl && ok; ++j) {
-            if (j < ntiles_cl) {
+        for (int j = 0; j <= ntiles_cta && ok; ++j) {
+            if (j < ntiles_cta) {
                 ok = mbar_wait_warp(&bars->k_full[ks_], kph);
                 const uint64_t kd = kdesc0 + (uint64_t)((ks_ * kTileBytes) >> 4);
 #pragma unroll
@@ -274,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     tc_commit_ew(&bars->s_full[t]);
                 }
                 if (!ok) break;
-                tc_commit_mc_ew(&bars->k_empty[ks_], all_mask);  // release the K slot cluster-wide
+                tc_commit_ew(&bars->k_empty[ks_]);  // release the K slot once both Q K^T have run
                 if (++ks_ == kKStages) {
                     ks_ = 0;
                     kph ^= 1;
@@ -300,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     tc_commit_ew(&bars->o_done[t][pb]);
                 }
                 if (!ok) break;
-                tc_commit_mc_ew(&bars->v_empty[vs_], all_mask);
+                tc_commit_ew(&bars->v_empty[vs_]);
                 if (++vs_ == kVStages) {
                     vs_ = 0;
                     vph ^= 1;
@@ -460,8 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                 // keys at or past the sequence end: zero their V rows, whatever the slots hold.
                 // Once V(j) has landed, every earlier reader of the slot has finished (its
                 // refill waited for all of them), and P V(j) of either tile is issued after
-                // this warpgroup's P(j) is complete.  (Every cluster member zeroes its own
-                // copy before releasing the slot.)
+                // this warpgroup's P(j) is complete.
                 const int s = j % kVStages;
                 if (__any_sync(0xffffffffu, !mbar_wait(&bars->v_full[s], (j / kVStages) & 1))) {
                     ok = false;
@@ -511,8 +491,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
-    // no member leaves while another may still multicast into its memory or release to it
-    cluster_sync_all();
 }
 
 }  // namespace
@@ -548,27 +526,14 @@ cudaError_t launch_prefill_tc(const PoolView& pool, const AttnArgs& a, cudaStrea
     const int tpt = kRows / t.group;
     const int tiles = std::max(1, (a.max_chunk + tpt - 1) / tpt);
     const int pairs = (tiles + 1) / 2;
-    // cluster over consecutive tile pairs of one (sequence, kv head): up to 4 members
-    static const int forced = [] {
-        const char* e = std::getenv("PA_PREFILL_CLUSTER");
-        return e ? std::atoi(e) : 0;
-    }();
-    int cs = forced > 0 ? forced : 4;
-    cs = std::max(1, std::min(cs, 8));
-    while (cs > 1 && cs > pairs) cs >>= 1;
-    const int gx = (pairs + cs - 1) / cs * cs;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(gx, pool.num_kv_heads, a.batch);
+    cfg.gridDim = dim3(pairs, pool.num_kv_heads, a.batch);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2] = {pdl_attribute(), {}};
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = cs;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, prefill_tc_kernel, pool.tm_k, pool.tm_v, t);
 }
 

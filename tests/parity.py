@@ -1,11 +1,14 @@
 """Run a workloads.PagedCase through the CUDA library and through the oracle, and compare.
 
 Tolerance (bf16 inputs, fp32 accumulation, bf16 output):
-  * absolute: |gpu - oracle| <= 1e-2 + ulp_bf16(oracle) / 2 for every element -- the 1e-2
-    bounds the computation; the half ulp is the final rounding of the result to bf16, which
-    no bf16 output can avoid (it alone exceeds 1e-2 once |o| >= 4);
+  * absolute: every element within max(1e-2, ulp_bf16(oracle) / 2) of the oracle.  The 1e-2
+    is the stated bound; the half ulp only takes over where the final rounding of the result
+    to bf16, which no bf16 output can avoid, alone exceeds it (|o| >= 4);
   * relative: per (token, head) row, max|gpu - oracle| / max|oracle| <= 2e-2.
 Rows whose oracle output is exactly zero (a sequence of length 0) must be exactly zero.
+
+Every comparison is recorded in REPORT (raw max-abs, row max-rel and their headroom), which
+the test session prints at its end.
 """
 from __future__ import annotations
 
@@ -19,6 +22,9 @@ from workloads import u16
 ATOL = 1e-2
 RTOL_ROW = 2e-2
 
+# (what, elements, raw max |gpu - oracle|, max row-relative error) of every comparison made
+REPORT = []
+
 
 def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
     """Half the spacing of bf16 numbers at |x| (8 significant bits)."""
@@ -28,17 +34,23 @@ def half_ulp_bf16(x: np.ndarray) -> np.ndarray:
 
 
 def compare(gpu: torch.Tensor, ref: np.ndarray, what: str, atol: float = ATOL, rtol_row: float = RTOL_ROW):
+    """Assert the tolerance above; returns (raw max-abs error, max row-relative error)."""
     g = gpu.detach().to("cpu", torch.float64).numpy().reshape(ref.shape)
     assert np.all(np.isfinite(g)), f"{what}: non-finite GPU output (read outside a sequence?)"
     diff = np.abs(g - ref)
-    excess = diff - half_ulp_bf16(ref)
-    max_abs = float(excess.max()) if diff.size else 0.0
+    max_abs = float(diff.max()) if diff.size else 0.0
+    bound = np.maximum(atol, half_ulp_bf16(ref))
+    over = diff > bound
     rows_d = diff.reshape(-1, ref.shape[-1]).max(axis=1) if diff.size else np.zeros(0)
     rows_r = np.abs(ref).reshape(-1, ref.shape[-1]).max(axis=1) if diff.size else np.zeros(0)
     zero = rows_r == 0
-    assert np.all(rows_d[zero] == 0), f"{what}: rows with an all-zero reference are not zero"
     rel = float((rows_d[~zero] / rows_r[~zero]).max()) if np.any(~zero) else 0.0
-    assert max_abs <= atol, f"{what}: max abs err beyond bf16 rounding {max_abs:.3e} > {atol}"
+    REPORT.append((what, int(diff.size), max_abs, rel))
+    assert np.all(rows_d[zero] == 0), f"{what}: rows with an all-zero reference are not zero"
+    if np.any(over):
+        i = np.unravel_index(int(np.argmax(diff - bound)), diff.shape)
+        raise AssertionError(f"{what}: {int(over.sum())} elements beyond max({atol}, half ulp); worst at {i}: "
+                             f"gpu {g[i]!r} oracle {ref[i]!r} (max abs err {max_abs:.3e})")
     assert rel <= rtol_row, f"{what}: max row-rel err {rel:.3e} > {rtol_row}"
     return max_abs, rel
 

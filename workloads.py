@@ -96,18 +96,6 @@ class PagedCase:
     def is_decode(self) -> bool:
         return all(c == 1 for c in self.q_lens)
 
-    def pool_after_append(self):
-        """Pool contents once the append has run (a plain scatter, for inputs only)."""
-        k = self.k_cache.clone()
-        v = self.v_cache.clone()
-        bs = self.block_size
-        for i, slot in enumerate(self.slot_mapping.tolist()):
-            if slot < 0:
-                continue
-            k[slot // bs, :, slot % bs, :] = self.k_new[i]
-            v[slot // bs, :, slot % bs, :] = self.v_new[i]
-        return k, v
-
     def kv_bytes(self) -> int:
         """Bytes of K and V that the attention must read, counted once per kv head."""
         esz = 2
