@@ -28,13 +28,16 @@ CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-s
 
 
 def build(source: Path = SOURCE, out: Path = LIB_PATH, force: bool = False) -> Path:
-    """Compile the oracle (plain C, gcc) if the shared object is missing or stale."""
+    """Compile the oracle (plain C, gcc) if the shared object is missing or stale: with
+    OpenMP where gcc has it (the row loops may then run on several threads), else without."""
     source, out = Path(source), Path(out)
     if not force and out.exists() and out.stat().st_mtime >= source.stat().st_mtime:
         return out
     out.parent.mkdir(parents=True, exist_ok=True)
     tmp = out.with_suffix(f".{os.getpid()}.tmp.so")
-    subprocess.run(["gcc", *CFLAGS, str(source), "-o", str(tmp), "-lm"], check=True)
+    r = subprocess.run(["gcc", *CFLAGS, "-fopenmp", str(source), "-o", str(tmp), "-lm"], capture_output=True)
+    if r.returncode != 0:
+        subprocess.run(["gcc", *CFLAGS, str(source), "-o", str(tmp), "-lm"], check=True)
     os.replace(tmp, out)
     return out
 
@@ -75,6 +78,15 @@ class Oracle:
         for f in ("pa_oracle_kv_append", "pa_oracle_decode", "pa_oracle_decode_partitions", "pa_oracle_combine",
                   "pa_oracle_prefill", "pa_oracle_prefill_rows"):
             getattr(L, f).restype = ctypes.c_int
+        L.pa_oracle_set_threads.argtypes = [_i32]
+        L.pa_oracle_set_threads.restype = ctypes.c_int
+        self.threads = self.set_threads(int(os.environ.get("PA_ORACLE_THREADS", os.cpu_count() or 1)))
+
+    def set_threads(self, n: int) -> int:
+        """Threads the per-row loops may use (1 if built without OpenMP); returns the count in
+        effect.  The results are the same bits for any count: each row is one thread's work."""
+        self.threads = int(self.lib.pa_oracle_set_threads(int(n)))
+        return self.threads
 
     @staticmethod
     def _check(rc: int, what: str):

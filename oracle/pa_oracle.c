@@ -37,16 +37,38 @@
  *
  * Every function returns 0 on success and a negative value on an invalid argument
  * (null pointer, bad shape, block id or slot outside the pool).
+ *
+ * Threads.  Every output row (one query head of one query token) is computed on its own,
+ * start to finish, by one thread; compiled with OpenMP, the loops over rows may hand rows to
+ * several threads (pa_oracle_set_threads), which changes neither the arithmetic nor its
+ * order within a row, so the results are the same bits for any thread count.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
 #define ORACLE_OK 0
 #define ORACLE_ERR_ARG (-1)
 #define ORACLE_ERR_RANGE (-2)
 #define ORACLE_ERR_NOMEM (-3)
+
+static int g_threads = 1;
+
+/* Threads the row loops may use (1 without OpenMP); returns the count now in effect. */
+int pa_oracle_set_threads(int32_t n) {
+#ifdef _OPENMP
+    g_threads = n > 0 ? n : 1;
+#else
+    (void)n;
+    g_threads = 1;
+#endif
+    return g_threads;
+}
 
 /* bf16 is the upper half of an IEEE binary32: widen the bits, then the value. */
 static double bf16_to_double(uint16_t bits) {
@@ -158,17 +180,19 @@ int pa_oracle_decode(const uint16_t *k_cache, const uint16_t *v_cache, int32_t n
         num_heads % num_kv_heads)
         return ORACLE_ERR_ARG;
     const int32_t g = num_heads / num_kv_heads;
-    for (int32_t b = 0; b < batch; ++b) {
+    for (int32_t b = 0; b < batch; ++b)
         if (seq_lens[b] < 0 || seq_lens[b] > max_blocks * block_size) return ORACLE_ERR_ARG;
-        for (int32_t h = 0; h < num_heads; ++h) {
-            double lse;
-            size_t row = (size_t)b * num_heads + h;
-            int rc = attend(&pool, block_tables + (size_t)b * max_blocks, max_blocks, h / g,
-                            q + row * head_dim, scale, 0, seq_lens[b], out + row * head_dim, &lse);
-            if (rc) return rc;
-        }
+    const long long rows = (long long)batch * num_heads;
+    int err = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) reduction(min : err)
+    for (long long row = 0; row < rows; ++row) {
+        const int32_t b = (int32_t)(row / num_heads), h = (int32_t)(row % num_heads);
+        double lse;
+        int rc = attend(&pool, block_tables + (size_t)b * max_blocks, max_blocks, h / g,
+                        q + (size_t)row * head_dim, scale, 0, seq_lens[b], out + (size_t)row * head_dim, &lse);
+        if (rc < err) err = rc;
     }
-    return ORACLE_OK;
+    return err;
 }
 
 /* Split-KV partitions: o_part [B, Hq, P, D] normalised per partition, lse_part [B, Hq, P]. */
@@ -182,25 +206,27 @@ int pa_oracle_decode_partitions(const uint16_t *k_cache, const uint16_t *v_cache
         num_heads <= 0 || num_heads % num_kv_heads || num_partitions < 1)
         return ORACLE_ERR_ARG;
     const int32_t g = num_heads / num_kv_heads;
-    for (int32_t b = 0; b < batch; ++b) {
+    for (int32_t b = 0; b < batch; ++b)
+        if (seq_lens[b] < 0 || seq_lens[b] > max_blocks * block_size) return ORACLE_ERR_ARG;
+    const long long rows = (long long)batch * num_heads;
+    int err = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) reduction(min : err)
+    for (long long row = 0; row < rows; ++row) {
+        const int32_t b = (int32_t)(row / num_heads), h = (int32_t)(row % num_heads);
         const int32_t L = seq_lens[b];
-        if (L < 0 || L > max_blocks * block_size) return ORACLE_ERR_ARG;
         const int32_t nb = (L + block_size - 1) / block_size;
         const int32_t per = (nb + num_partitions - 1) / num_partitions;
-        for (int32_t h = 0; h < num_heads; ++h) {
-            size_t row = (size_t)b * num_heads + h;
-            for (int32_t j = 0; j < num_partitions; ++j) {
-                int32_t t0 = j * per * block_size;
-                int32_t t1 = (j + 1) * per * block_size;
-                if (t1 > L) t1 = L;
-                size_t pr = row * num_partitions + j;
-                int rc = attend(&pool, block_tables + (size_t)b * max_blocks, max_blocks, h / g,
-                                q + row * head_dim, scale, t0, t1, o_part + pr * head_dim, lse_part + pr);
-                if (rc) return rc;
-            }
+        for (int32_t j = 0; j < num_partitions; ++j) {
+            int32_t t0 = j * per * block_size;
+            int32_t t1 = (j + 1) * per * block_size;
+            if (t1 > L) t1 = L;
+            size_t pr = (size_t)row * num_partitions + j;
+            int rc = attend(&pool, block_tables + (size_t)b * max_blocks, max_blocks, h / g,
+                            q + (size_t)row * head_dim, scale, t0, t1, o_part + pr * head_dim, lse_part + pr);
+            if (rc < err) err = rc;
         }
     }
-    return ORACLE_OK;
+    return err;
 }
 
 /* Log-sum-exp merge of P partitions into out [B, Hq, D]. */
@@ -247,23 +273,31 @@ int pa_oracle_prefill_rows(const uint16_t *k_cache, const uint16_t *v_cache, int
     const int32_t g = num_heads / num_kv_heads;
     const int32_t total = cu_q_lens[batch];
     const int32_t n = row_tokens ? nrows : total * num_heads;
+    int err = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(g_threads) reduction(min : err)
     for (int32_t r = 0; r < n; ++r) {
         int32_t tok = row_tokens ? row_tokens[r] : r / num_heads;
         int32_t h = row_tokens ? row_heads[r] : r % num_heads;
-        if (tok < 0 || tok >= total || h < 0 || h >= num_heads) return ORACLE_ERR_ARG;
+        if (tok < 0 || tok >= total || h < 0 || h >= num_heads) {
+            err = ORACLE_ERR_ARG;
+            continue;
+        }
         int32_t s = 0;
         while (!(cu_q_lens[s] <= tok && tok < cu_q_lens[s + 1])) ++s;
         const int32_t L = seq_lens[s];
         const int32_t C = cu_q_lens[s + 1] - cu_q_lens[s];
-        if (L < C || L > max_blocks * block_size) return ORACLE_ERR_ARG;
+        if (L < C || L > max_blocks * block_size) {
+            err = ORACLE_ERR_ARG;
+            continue;
+        }
         const int32_t pos = L - C + (tok - cu_q_lens[s]);
         double lse;
         int rc = attend(&pool, block_tables + (size_t)s * max_blocks, max_blocks, h / g,
                         q + ((size_t)tok * num_heads + h) * head_dim, scale, 0, pos + 1,
                         out + (size_t)r * head_dim, &lse);
-        if (rc) return rc;
+        if (rc < err) err = rc;
     }
-    return ORACLE_OK;
+    return err;
 }
 
 int pa_oracle_prefill(const uint16_t *k_cache, const uint16_t *v_cache, int32_t num_blocks, int32_t block_size,

@@ -15,6 +15,7 @@
 // computes S = Q K^T with mma.m16n8k16 (Q fragments stay in registers), masks, updates
 // the running max / sum (online softmax in base 2, fp32), rounds P to bf16 and
 // accumulates O += P V with the same MMA, reading K and V with ldmatrix (V transposed).
+// The running sum adds the bf16-rounded P, the very weights the P V product uses.
 #pragma once
 
 #include "pa_device.cuh"
@@ -137,10 +138,10 @@ __device__ __forceinline__ RowUpdate row_update(float& m, float& l, float s0, fl
     const float base = mn == -INFINITY ? 0.f : mn;  // a row that has seen no key yet
     RowUpdate u;
     u.alpha = fast_exp2(m - base);
-    x0 = fast_exp2(x0 - base);
-    x1 = fast_exp2(x1 - base);
-    x2 = fast_exp2(x2 - base);
-    x3 = fast_exp2(x3 - base);
+    x0 = round_bf16(fast_exp2(x0 - base));
+    x1 = round_bf16(fast_exp2(x1 - base));
+    x2 = round_bf16(fast_exp2(x2 - base));
+    x3 = round_bf16(fast_exp2(x3 - base));
     l = l * u.alpha + ((x0 + x1) + (x2 + x3));
     m = mn;
     u.p01 = pack_bf16x2(x0, x1);
@@ -308,7 +309,8 @@ __device__ __forceinline__ void load_q_rows(uint32_t (&qb)[NT][D / 16][2], const
 }
 
 // One head column's update from this thread's two tokens (x0: token lane/4, x8: lane/4+8);
-// returns alpha and writes the two probabilities back into x0, x8.
+// returns alpha and writes the two probabilities back into x0, x8, already rounded to bf16
+// (the P V operand), which is also what the running sum adds.
 __device__ __forceinline__ float head_update(float& m, float& l, float& x0, float& x8) {
     float mx = fmaxf(x0, x8);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
@@ -317,8 +319,8 @@ __device__ __forceinline__ float head_update(float& m, float& l, float& x0, floa
     const float mn = fmaxf(m, mx);
     const float base = mn == -INFINITY ? 0.f : mn;
     const float alpha = fast_exp2(m - base);
-    x0 = fast_exp2(x0 - base);
-    x8 = fast_exp2(x8 - base);
+    x0 = round_bf16(fast_exp2(x0 - base));
+    x8 = round_bf16(fast_exp2(x8 - base));
     l = l * alpha + (x0 + x8);
     m = mn;
     return alpha;

@@ -175,6 +175,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// x rounded to the nearest bf16 (ties to even), as a float.  The softmax rounds P to bf16 for
+// the P V product; summing the normaliser from the same rounded values keeps numerator and
+// denominator consistent, so the rounding perturbs the weights but not their total.
+__device__ __forceinline__ float round_bf16(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// The two bf16 halves of a packed pair as floats (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
 __device__ __forceinline__ uint32_t ld_u32(const void* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
 // 2^x on the special-function unit (PTX ex2.approx; 2^-inf = +0)

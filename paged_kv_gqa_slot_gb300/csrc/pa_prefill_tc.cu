@@ -407,7 +407,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             const float nbase = m_used == -INFINITY ? 0.f : -m_used;
             uint8_t* prow = smem + kOffP + (t * kPBufs + pb) * kPBytes;
             // p = 2^(s |scale| log2(e) - m): one packed multiply-add per two keys, then the
-            // special-function unit; sums in four packed chains.
+            // special-function unit; P is rounded to bf16 for P V, and the row sum adds those
+            // rounded values (in four packed chains), so the weights P V uses sum to l.
             float ls[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) ls[e] = 0.f;
@@ -427,13 +428,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
                     for (int e = 0; e < 8; ++e)
                         if (cc * 8 + e > lim) pp[e] = 0.f;
                 }
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) add_x2(ls[e], ls[e + 1], pp[e], pp[e + 1]);
                 uint4 v;
                 v.x = pack_bf16x2(pp[0], pp[1]);
                 v.y = pack_bf16x2(pp[2], pp[3]);
                 v.z = pack_bf16x2(pp[4], pp[5]);
                 v.w = pack_bf16x2(pp[6], pp[7]);
+                add_x2(ls[0], ls[1], bf16_lo(v.x), bf16_hi(v.x));
+                add_x2(ls[2], ls[3], bf16_lo(v.y), bf16_hi(v.y));
+                add_x2(ls[4], ls[5], bf16_lo(v.z), bf16_hi(v.z));
+                add_x2(ls[6], ls[7], bf16_lo(v.w), bf16_hi(v.w));
                 *reinterpret_cast<uint4*>(prow + swz128(r, cc)) = v;
             }
             l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));

@@ -11,10 +11,11 @@ import oracle
 import oracle_pins as pins
 
 MUTANTS = {
-    "kv_head_modulo": ("h / g,\n                            q + row * head_dim, scale, 0, seq_lens[b]",
-                       "h % num_kv_heads,\n                            q + row * head_dim, scale, 0, seq_lens[b]"),
+    "kv_head_modulo": ("h / g,\n                        q + (size_t)row * head_dim, scale, 0, seq_lens[b]",
+                       "h % num_kv_heads,\n                        q + (size_t)row * head_dim, scale, 0, seq_lens[b]"),
     "scale_dropped": ("s[t - t_begin] = scale * dot;", "s[t - t_begin] = dot;"),
-    "decode_drops_last_key": ("scale, 0, seq_lens[b], out + row * head_dim", "scale, 0, seq_lens[b] - 1, out + row * head_dim"),
+    "decode_drops_last_key": ("scale, 0, seq_lens[b], out + (size_t)row * head_dim",
+                              "scale, 0, seq_lens[b] - 1, out + (size_t)row * head_dim"),
     "head_ignored_in_pool": ("((size_t)blk * pool->num_kv_heads + kvh) * pool->block_size + off",
                              "((size_t)blk * pool->num_kv_heads + 0) * pool->block_size + off"),
     "offset_from_block_index": ("int32_t off = t % pool->block_size;", "int32_t off = (t / pool->block_size) % pool->block_size;"),
@@ -28,7 +29,7 @@ MUTANTS = {
     "softmax_sign": ("double w = exp(s[t - t_begin] - m);", "double w = exp(m - s[t - t_begin]);"),
     "partition_size_floor": ("const int32_t per = (nb + num_partitions - 1) / num_partitions;",
                              "const int32_t per = nb / num_partitions > 0 ? nb / num_partitions : 1;"),
-    "q_row_of_kv_head": ("q + row * head_dim, scale, 0, seq_lens[b]",
+    "q_row_of_kv_head": ("q + (size_t)row * head_dim, scale, 0, seq_lens[b]",
                          "q + ((size_t)b * num_heads + (h / g) * g) * head_dim, scale, 0, seq_lens[b]"),
 }
 
