@@ -285,6 +285,37 @@ int pa_decode_splitkv(const pa_pool* pool, const void* q, const int32_t* block_t
     return from_cuda(launch_decode_splitkv(v, a, (cudaStream_t)stream));
 }
 
+int pa_decode_splitkv_merged(const pa_pool* pool, const void* q, const int32_t* block_tables, int32_t max_blocks,
+                             const int32_t* seq_lens, int32_t batch, int32_t num_heads, float scale,
+                             int32_t num_partitions, float* ws_o, float* ws_lse, uint32_t* arrivals, void* out,
+                             pa_stream_t stream) {
+    PoolView v;
+    int rc = check_attn(pool, &v, q, block_tables, max_blocks, seq_lens, batch, num_heads, scale, out);
+    if (rc) return rc;
+    if (num_partitions < 1 || num_partitions > 4096) return PA_ERR_INVALID_ARG;
+    if (batch == 0) return PA_OK;
+    if (!ws_o || !ws_lse || !arrivals || !aligned16(ws_o)) return PA_ERR_INVALID_ARG;
+    if (num_heads / v.num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
+    rc = check_pool(pool, &v, true);
+    if (rc) return rc;
+    AttnArgs a{};
+    a.q = q;
+    a.block_tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.ws_o = ws_o;
+    a.ws_lse = ws_lse;
+    a.arrivals = arrivals;
+    a.status = device_status_ptr();
+    if (!a.status) return PA_ERR_CUDA;
+    a.batch = batch;
+    a.num_heads = num_heads;
+    a.max_blocks = max_blocks;
+    a.num_partitions = num_partitions;
+    a.scale = scale;
+    return from_cuda(launch_decode_splitkv(v, a, (cudaStream_t)stream));
+}
+
 int pa_combine(const float* ws_o, const float* ws_lse, int32_t batch, int32_t num_heads, int32_t head_dim,
                int32_t num_partitions, void* out, pa_stream_t stream) {
     if (batch < 0 || num_heads <= 0 || num_partitions < 1 || num_partitions > 4096) return PA_ERR_INVALID_ARG;

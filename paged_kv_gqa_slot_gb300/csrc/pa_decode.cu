@@ -15,7 +15,11 @@
 //     cluster and merges their partials through distributed shared memory (no
 //     workspace, one launch) -- used when batch x kv heads is too small to fill the GPU;
 //   * pa_decode_splitkv writes each partition's normalised O_p and lse_p to the caller's
-//     workspace for pa_combine.
+//     workspace for pa_combine;
+//   * pa_decode_splitkv_merged does the same and then merges in the same launch: every
+//     partition (CTA, or cluster) of a (sequence, kv head) counts itself in on an arrival
+//     counter once its results are written, and the one that arrives last -- it never waits
+//     for the others -- reads all P partitions back and writes the bf16 output.
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
@@ -73,7 +77,72 @@ struct DecodeArgs {
     const int32_t* cu_q_lens;  // multi-query: chunk of query tokens of each sequence [B+1]
     void* k_pool;  // the pool, for the fused append's row write
     void* v_pool;
+    unsigned* arrivals;  // split-KV merged in the launch: [B * Hkv] counters (zero between calls), or null
 };
+
+// Split-KV merged in the launch.  Called by every thread of the CTA that completed one
+// partition of (sequence b, kv head kvh) after its results are in ws_o / ws_lse: the CTA counts
+// itself in on the (b, kvh) arrival counter, and the one that arrives last (no CTA ever waits)
+// reads the P partitions back from L2 and writes the merged bf16 output of the group's heads:
+//   M = max_p lse_p,  out = sum_p e^{lse_p - M} O_p / sum_p e^{lse_p - M}.
+// The last arrival sets the counter back to zero for the next call.
+template <int D>
+__device__ __forceinline__ void merge_if_last(const DecodeArgs& a, int b, int kvh, int parts, int R) {
+    __shared__ unsigned s_last;
+    __threadfence();  // this thread's ws_o / ws_lse writes are visible GPU-wide before the count
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned* cnt = a.arrivals + (size_t)b * a.num_kv_heads + kvh;
+        const unsigned prev = atomicAdd(cnt, 1u);
+        if (prev >= (unsigned)parts) atomicOr(a.status, kDevOutOfRange);  // counter was not zero at entry
+        const bool last = prev == (unsigned)parts - 1;
+        if (last) atomicExch(cnt, 0u);
+        s_last = last ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();  // the other partitions' results, counted in before us, are visible now
+    constexpr int kQuads = D / 4;
+    constexpr int kBatch = 8;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int h = warp; h < R; h += kThreads / 32) {
+        const size_t row = (size_t)b * a.num_heads + (size_t)kvh * a.group + h;
+        const float* lse = a.ws_lse + row * parts;
+        const float4* op = reinterpret_cast<const float4*>(a.ws_o + row * parts * D) + lane;
+        float M = -INFINITY;
+        for (int p = lane; p < parts; p += 32) M = fmaxf(M, __ldcg(lse + p));
+        M = warp_max(M);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float den = 0.f;
+        if (M != -INFINITY) {
+            for (int p0 = 0; p0 < parts; p0 += kBatch) {
+                float lp[kBatch];
+                float4 v[kBatch];
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const int p = p0 + k;
+                    lp[k] = p < parts ? __ldcg(lse + p) : -INFINITY;
+                    v[k] = (p < parts && lane < kQuads) ? __ldcg(op + (size_t)p * kQuads) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int k = 0; k < kBatch; ++k) {
+                    const float w = lp[k] == -INFINITY ? 0.f : fast_exp2((lp[k] - M) * kLog2e);  // empty: weight 0
+                    den += w;
+                    acc.x += w * v[k].x;
+                    acc.y += w * v[k].y;
+                    acc.z += w * v[k].z;
+                    acc.w += w * v[k].w;
+                }
+            }
+        }
+        if (lane < kQuads) {
+            const float inv = den > 0.f ? 1.f / den : 0.f;
+            __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + row * D + lane * 4);
+            dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        }
+    }
+}
 
 template <int D, int NT, bool SPLIT, bool MQ>
 __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -288,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             a.ws_o[row * D + dd] = den > 0.f ? cta[32 + e] / den : 0.f;
             if (dd == 0) a.ws_lse[row] = den > 0.f ? (cta[h] + log2f(den)) * kLn2 : -INFINITY;
         }
+        if (a.arrivals != nullptr) merge_if_last<D>(a, b, kvh, parts, R);
         return;
     }
     // element e = row * D + d of this CTA's output -> its place in out
@@ -363,7 +433,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
         }
     }
+    if (SPLIT && a.arrivals != nullptr) __threadfence();  // this CTA's O_p slice, before the count
     cluster.sync();  // keep this CTA's partial alive until every reader is done
+    // the partition is complete once every member has passed the barrier: its rank 0 counts it in
+    if (SPLIT && a.arrivals != nullptr && rank == 0) merge_if_last<D>(a, b, kvh, parts, R);
 }
 
 // out[r, :] = sum_p exp(lse_p - M) O_p / sum_p exp(lse_p - M) with M = max_p lse_p.
@@ -492,6 +565,7 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int grid_x, int 
     da.k_pool = pool.k;
     da.v_pool = pool.v;
     da.cu_q_lens = MQ ? a.cu_q_lens : nullptr;
+    da.arrivals = SPLIT ? a.arrivals : nullptr;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, pool.num_kv_heads, a.batch);

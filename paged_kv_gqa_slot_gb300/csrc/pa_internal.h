@@ -57,6 +57,9 @@ struct AttnArgs {
     const void* k_new;
     const void* v_new;
     const int64_t* slots;
+    // split-KV only, merged in the launch (null: partials only, for pa_combine): one arrival
+    // counter per (sequence, kv head), zero between calls
+    unsigned* arrivals;
 };
 
 const DeviceInfo& device_info();

@@ -170,6 +170,73 @@ def test_splitkv_ragged_and_empty_partitions(P):
     _check_split(case, P)
 
 
+def _check_merged(case, P, calls=2):
+    """pa_decode_splitkv_merged against the oracle's decode, `calls` times in a row on the same
+    counters (each call must leave them zero), and its partials against the oracle's."""
+    g = GpuCase(case)
+    B, Hq, D = case.q.shape
+    ws_o = torch.empty((B, Hq, P, D), dtype=torch.float32, device="cuda")
+    ws_lse = torch.empty((B, Hq, P), dtype=torch.float32, device="cuda")
+    arrivals = torch.zeros(B * case.num_kv_heads, dtype=torch.int32, device="cuda")
+    k, v = oracle_pool(case)
+    orc = oracle.load()
+    ref = orc.decode(k, v, u16(case.q), case.block_tables.numpy(), case.seq_lens.numpy(), case.scale)
+    for call in range(calls):
+        out = torch.full_like(g.q, float("nan"))
+        pa.pa_decode_splitkv_merged(g.pool, g.q, g.bt, g.sl, case.scale, P, ws_o, ws_lse, arrivals, out)
+        check_status_clean(f"merged split P={P}, call {call}")
+        compare(out, ref, f"{case.name} P={P} merged in the launch, call {call}")
+        assert int(arrivals.abs().sum()) == 0, "arrival counters not back to zero"
+    o_ref, lse_ref = orc.decode_partitions(k, v, u16(case.q), case.block_tables.numpy(), case.seq_lens.numpy(),
+                                           case.scale, P)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(ws_lse.cpu().numpy()), fin)
+    compare(ws_o[torch.from_numpy(fin).to(ws_o.device)], o_ref[fin], f"{case.name} P={P} merged: partial O")
+    return out
+
+
+@pytest.mark.parametrize("P", [8, 19, 32])
+def test_splitkv_merged_4x8192(P):
+    _check_merged(W.splitkv_decode(1004, 4, 8192), P)
+
+
+@pytest.mark.parametrize("P", [8, 32])
+def test_splitkv_merged_1x32768(P):
+    """Few (sequence, kv head) pairs: each partition runs on a cluster of CTAs whose rank 0
+    counts the partition in once the whole cluster has written it."""
+    _check_merged(W.splitkv_decode(1004, 1, 32768), P)
+
+
+@pytest.mark.parametrize("P", [1, 3, 64])
+def test_splitkv_merged_ragged_and_empty(P):
+    """Ragged lengths (partitions past a short sequence are empty) and a zero-length
+    sequence, whose output row must be zero."""
+    case = W.paged_case(name="merged_ragged", seed=4300 + P, seq_lens=[1, 300, 0, 77, 1000, 16],
+                        q_lens=[1] * 6, new_lens=[1, 1, 0, 1, 1, 1], num_heads=32, num_kv_heads=8, head_dim=128,
+                        num_blocks=256)
+    out = _check_merged(case, P)
+    assert torch.all(out[2] == 0)
+
+
+def test_splitkv_merged_flags_a_dirty_counter():
+    """A counter that is not zero at entry (e.g. left by an aborted call) is reported as
+    PA_DEV_OUT_OF_RANGE; the other (sequence, kv head) pairs are merged as usual."""
+    case = W.random_case(4400, batch=3, num_heads=32, num_kv_heads=8, head_dim=128, min_len=100, max_len=400)
+    g = GpuCase(case)
+    B, Hq, D = case.q.shape
+    P = 4
+    ws_o = torch.empty((B, Hq, P, D), dtype=torch.float32, device="cuda")
+    ws_lse = torch.empty((B, Hq, P), dtype=torch.float32, device="cuda")
+    arrivals = torch.zeros(B * case.num_kv_heads, dtype=torch.int32, device="cuda")
+    arrivals[5] = 7  # sequence 0, kv head 5
+    out = torch.zeros_like(g.q)
+    pa.pa_decode_splitkv_merged(g.pool, g.q, g.bt, g.sl, case.scale, P, ws_o, ws_lse, arrivals, out)
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    ref = oracle_decode(case)
+    compare(out[1:], ref[1:], "merged split beside a dirty counter")
+    compare(out[0, :20], ref[0, :20], "merged split, clean kv heads of the same sequence")
+
+
 def test_splitkv_one_partition_equals_decode():
     case = W.random_case(4100, batch=4, num_heads=32, num_kv_heads=8, head_dim=128, min_len=50, max_len=200)
     g = GpuCase(case)
