@@ -92,6 +92,22 @@ int pa_kv_append(const pa_pool *pool, const void *k_new, const void *v_new, cons
                  int32_t num_tokens, pa_stream_t stream);
 
 /*
+ * pa_kv_copy -- copy whole pool rows (every kv head, K and V): for t in [0, n),
+ *   k_cache[dst / 16, h, dst % 16, :] = k_cache[src / 16, h, src % 16, :]  (and v likewise)
+ * with src = src_slots[t], dst = dst_slots[t].  This is the copy on write of a prefix-cache
+ * hit that ends inside a cached block ("Qwen3-4B / 8B / 32B", "Warm Prefix-Cache TTFT": a
+ * warm request reuses the cached K/V of its prompt prefix): pa_bm_admit_cow returns the slot
+ * pairs, and the copy must precede, on the same stream, the append of the request's own
+ * tokens and any attention call that reads them.
+ *   src_slots, dst_slots  [n] int64 device arrays; a pair with a negative slot is skipped, one
+ *                         past the pool is skipped and sets PA_DEV_OUT_OF_RANGE.  A dst slot
+ *                         that is also some pair's src slot is a caller error.
+ * Bit-exact copy.
+ */
+int pa_kv_copy(const pa_pool *pool, const int64_t *src_slots, const int64_t *dst_slots, int32_t n,
+               pa_stream_t stream);
+
+/*
  * pa_decode -- one query token per sequence attends to keys [0, seq_lens[b]).
  * ("Qwen3-4B / 8B / 32B", "Architecture Notes": GQA over a paged KV cache; the query is
  * the newest token, already appended.)
@@ -277,6 +293,24 @@ void pa_bm_destroy(pa_blockmgr *bm);
 int pa_bm_admit(pa_blockmgr *bm, int64_t request_id, const int32_t *tokens, int32_t n_tokens,
                 int32_t max_new_tokens, int32_t *block_table, int32_t table_cap, int32_t *n_blocks,
                 int32_t *n_cached_tokens);
+
+/*
+ * pa_bm_admit_cow -- pa_bm_admit that also reuses a prefix hit ending inside a block.  After
+ * the prompt's matching full blocks, the cached block that follows the same prefix and whose
+ * leading tokens match the prompt's next tokens longest (k of them, 1 <= k <= 15, leaving the
+ * prompt's last token to compute) lends its first k rows: they are to be copied into the
+ * request's own block at that position (its table entry n_cached_tokens / 16), a copy on
+ * write, since a cached block is never written.
+ *   copy_src, copy_dst  out: n_copy slot pairs (block_size - 1 entries of room) for pa_kv_copy,
+ *                       which must run before the request's tokens [n_cached_tokens, ...) are
+ *                       appended and attended; n_copy = 0 when there is no partial hit
+ *   n_cached_tokens     out: tokens whose K/V is in the pool once that copy has run (any count)
+ * The source block is held (one reference) until the request is released, so no other
+ * request can take it before the copy.  Other arguments and results as pa_bm_admit.
+ */
+int pa_bm_admit_cow(pa_blockmgr *bm, int64_t request_id, const int32_t *tokens, int32_t n_tokens,
+                    int32_t max_new_tokens, int32_t *block_table, int32_t table_cap, int32_t *n_blocks,
+                    int32_t *n_cached_tokens, int64_t *copy_src, int64_t *copy_dst, int32_t *n_copy);
 
 /*
  * Append n_new generated tokens to the request's token list (within its reserved lifetime)

@@ -20,7 +20,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_append_decode", "pa_decode_splitkv", "pa_decode_splitkv_merged",
+__all__ = ["PaPool", "pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decode", "pa_decode_splitkv", "pa_decode_splitkv_merged",
            "pa_combine", "pa_prefill_chunked",
            "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "pa_splitkv_num_partitions",
            "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes", "PagedAttnError",
@@ -30,11 +30,11 @@ __all__ = ["PaPool", "pa_kv_append", "pa_decode", "pa_append_decode", "pa_decode
 BLOCK_SIZE = 16
 PKG = Path(__file__).resolve().parent
 _LIB_PATH = PKG / "libpagedattn.so"
-EXPORTED_SYMBOLS = ("pa_kv_append", "pa_decode", "pa_append_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv",
+EXPORTED_SYMBOLS = ("pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv",
                     "pa_decode_splitkv_merged", "pa_combine",
                     "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_splitkv_num_partitions",
                     "pa_status_str", "pa_version", "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes",
-                    "pa_kv_block_bytes", "pa_kv_budget_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_admit",
+                    "pa_kv_block_bytes", "pa_kv_budget_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_admit", "pa_bm_admit_cow",
                     "pa_bm_commit", "pa_bm_release", "pa_bm_slots", "pa_bm_stats")
 
 PA_OK = 0
@@ -80,6 +80,7 @@ def library() -> ctypes.CDLL:
     pool = ctypes.POINTER(_PaPoolC)
     sig = {
         "pa_kv_append": (ctypes.c_int, [pool, P, P, P, I32, P]),
+        "pa_kv_copy": (ctypes.c_int, [pool, P, P, I32, P]),
         "pa_decode": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, P, P]),
         "pa_append_decode": (ctypes.c_int, [pool, P, P, P, P, P, I32, P, I32, I32, F32, P, P]),
         "pa_splitkv_workspace_bytes": (SZ, [I32, I32, I32, I32]),
@@ -98,6 +99,7 @@ def library() -> ctypes.CDLL:
         "pa_bm_create": (P, [I32, I32, I32]),
         "pa_bm_destroy": (None, [P]),
         "pa_bm_admit": (ctypes.c_int, [P, ctypes.c_int64, P, I32, I32, P, I32, P, P]),
+        "pa_bm_admit_cow": (ctypes.c_int, [P, ctypes.c_int64, P, I32, I32, P, I32, P, P, P, P, P]),
         "pa_bm_commit": (ctypes.c_int, [P, ctypes.c_int64, P, I32, I32]),
         "pa_bm_release": (ctypes.c_int, [P, ctypes.c_int64]),
         "pa_bm_slots": (ctypes.c_int, [P, ctypes.c_int64, I32, I32, P]),
@@ -191,6 +193,16 @@ def pa_kv_append(pool: PaPool, k_new: torch.Tensor, v_new: torch.Tensor, slot_ma
                                 _dev(v_new, torch.bfloat16, "v_new") if T else None,
                                 _dev(slot_mapping, torch.int64, "slot_mapping") if T else None, T, _stream(stream))
     _check(rc, "pa_kv_append")
+
+
+def pa_kv_copy(pool: PaPool, src_slots: torch.Tensor, dst_slots: torch.Tensor, stream=None) -> None:
+    """Copy pool rows src_slots[t] -> dst_slots[t] (K and V, every kv head)."""
+    n = int(src_slots.numel())
+    if dst_slots.numel() != n:
+        raise ValueError(f"src_slots / dst_slots: need equal lengths, got {n} / {dst_slots.numel()}")
+    rc = library().pa_kv_copy(pool.ref, _dev(src_slots, torch.int64, "src_slots") if n else None,
+                              _dev(dst_slots, torch.int64, "dst_slots") if n else None, n, _stream(stream))
+    _check(rc, "pa_kv_copy")
 
 
 def pa_decode(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
@@ -396,6 +408,25 @@ class BlockManager:
             return None
         _check(rc, "pa_bm_admit")
         return table[:nb.value].copy(), nc.value
+
+    def admit_cow(self, request_id: int, tokens, max_new_tokens: int):
+        """(block_table, n_cached_tokens, copy_src, copy_dst), or None when rejected: a prefix
+        hit may end inside a block, whose leading rows copy_src -> copy_dst (slot arrays for
+        pa_kv_copy) must be copied before the request's own tokens are appended."""
+        np = self._np
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        cap = (len(toks) + max_new_tokens + self.block_size - 1) // self.block_size
+        table = np.empty(max(cap, 1), dtype=np.int32)
+        src = np.empty(self.block_size, dtype=np.int64)
+        dst = np.empty(self.block_size, dtype=np.int64)
+        nb, nc, ncp = ctypes.c_int32(0), ctypes.c_int32(0), ctypes.c_int32(0)
+        rc = library().pa_bm_admit_cow(self._h, request_id, toks.ctypes.data, len(toks), max_new_tokens,
+                                       table.ctypes.data, len(table), ctypes.byref(nb), ctypes.byref(nc),
+                                       src.ctypes.data, dst.ctypes.data, ctypes.byref(ncp))
+        if rc == PA_ERR_REJECTED:
+            return None
+        _check(rc, "pa_bm_admit_cow")
+        return table[:nb.value].copy(), nc.value, src[:ncp.value].copy(), dst[:ncp.value].copy()
 
     def commit(self, request_id: int, new_tokens, computed: int):
         np = self._np

@@ -184,6 +184,20 @@ int pa_kv_append(const pa_pool* pool, const void* k_new, const void* v_new, cons
     return from_cuda(launch_kv_append(v, k_new, v_new, slot_mapping, num_tokens, st, (cudaStream_t)stream));
 }
 
+int pa_kv_copy(const pa_pool* pool, const int64_t* src_slots, const int64_t* dst_slots, int32_t n,
+               pa_stream_t stream) {
+    PoolView v;
+    int rc = check_pool(pool, &v, false);
+    if (rc) return rc;
+    if (n < 0) return PA_ERR_INVALID_ARG;
+    if (n == 0) return PA_OK;
+    if (!src_slots || !dst_slots) return PA_ERR_INVALID_ARG;
+    if ((long long)n * 2 * v.num_kv_heads * (v.head_dim / 8) >= (1LL << 31)) return PA_ERR_INVALID_ARG;
+    unsigned* st = device_status_ptr();
+    if (!st) return PA_ERR_CUDA;
+    return from_cuda(launch_kv_copy(v, src_slots, dst_slots, n, st, (cudaStream_t)stream));
+}
+
 static int check_attn(const pa_pool* pool, PoolView* v, const void* q, const int32_t* block_tables,
                       int32_t max_blocks, const int32_t* seq_lens, int32_t batch, int32_t num_heads, float scale,
                       const void* out) {

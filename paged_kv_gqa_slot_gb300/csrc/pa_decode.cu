@@ -81,63 +81,73 @@ struct DecodeArgs {
 };
 
 // Split-KV merged in the launch.  Called by every thread of the CTA that completed one
-// partition of (sequence b, kv head kvh) after its results are in ws_o / ws_lse: the CTA counts
-// itself in on the (b, kvh) arrival counter, and the one that arrives last (no CTA ever waits)
-// reads the P partitions back from L2 and writes the merged bf16 output of the group's heads:
-//   M = max_p lse_p,  out = sum_p e^{lse_p - M} O_p / sum_p e^{lse_p - M}.
-// The last arrival sets the counter back to zero for the next call.
+// partition of (sequence b, kv head kvh) after its results are in ws_o / ws_lse (and, for a
+// cluster, after the barrier that follows every member's writes): the CTA counts itself in on
+// the (b, kvh) arrival counter with one acquire-release atomic, and the one that arrives last
+// (no CTA ever waits) reads the P partitions back from L2 and writes the merged bf16 output of
+// the group's heads:
+//   M = max_p lse_p,  w_p = e^{lse_p - M},  out = sum_p w_p O_p / sum_p w_p.
+// The last arrival sets the counter back to zero for the next call.  `scratch` is `room`
+// floats (>= parts + 1) of this CTA's shared memory that nothing else uses any more.
 template <int D>
-__device__ __forceinline__ void merge_if_last(const DecodeArgs& a, int b, int kvh, int parts, int R) {
+__device__ __forceinline__ void merge_if_last(const DecodeArgs& a, int b, int kvh, int parts, int R, float* scratch,
+                                              int room) {
     __shared__ unsigned s_last;
-    __threadfence();  // this thread's ws_o / ws_lse writes are visible GPU-wide before the count
-    __syncthreads();
+    __syncthreads();  // every write of this CTA's partition happens before thread 0's release
     if (threadIdx.x == 0) {
         unsigned* cnt = a.arrivals + (size_t)b * a.num_kv_heads + kvh;
-        const unsigned prev = atomicAdd(cnt, 1u);
+        unsigned prev;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
         if (prev >= (unsigned)parts) atomicOr(a.status, kDevOutOfRange);  // counter was not zero at entry
         const bool last = prev == (unsigned)parts - 1;
         if (last) atomicExch(cnt, 0u);
         s_last = last ? 1u : 0u;
     }
-    __syncthreads();
+    __syncthreads();  // thread 0's acquire orders the other partitions' results before our reads
     if (!s_last) return;
-    __threadfence();  // the other partitions' results, counted in before us, are visible now
     constexpr int kQuads = D / 4;
-    constexpr int kBatch = 8;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int h = warp; h < R; h += kThreads / 32) {
-        const size_t row = (size_t)b * a.num_heads + (size_t)kvh * a.group + h;
-        const float* lse = a.ws_lse + row * parts;
-        const float4* op = reinterpret_cast<const float4*>(a.ws_o + row * parts * D) + lane;
-        float M = -INFINITY;
-        for (int p = lane; p < parts; p += 32) M = fmaxf(M, __ldcg(lse + p));
-        M = warp_max(M);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float den = 0.f;
-        if (M != -INFINITY) {
-            for (int p0 = 0; p0 < parts; p0 += kBatch) {
-                float lp[kBatch];
-                float4 v[kBatch];
-#pragma unroll
-                for (int k = 0; k < kBatch; ++k) {
-                    const int p = p0 + k;
-                    lp[k] = p < parts ? __ldcg(lse + p) : -INFINITY;
-                    v[k] = (p < parts && lane < kQuads) ? __ldcg(op + (size_t)p * kQuads) : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-                for (int k = 0; k < kBatch; ++k) {
-                    const float w = lp[k] == -INFINITY ? 0.f : fast_exp2((lp[k] - M) * kLog2e);  // empty: weight 0
-                    den += w;
-                    acc.x += w * v[k].x;
-                    acc.y += w * v[k].y;
-                    acc.z += w * v[k].z;
-                    acc.w += w * v[k].w;
-                }
+    // heads per pass: their weights [hp][parts] and sums [hp] fit the scratch
+    const int hp = max(1, min(R, room / (parts + 1)));
+    for (int h0 = 0; h0 < R; h0 += hp) {
+        const int nh = min(hp, R - h0);
+        const size_t row0 = (size_t)b * a.num_heads + (size_t)kvh * a.group + h0;
+        float* w = scratch;                 // [nh][parts]: lse, then the merge weights
+        float* den = scratch + nh * parts;  // [nh]
+        __syncthreads();  // the previous pass is done with the scratch
+        for (int i = threadIdx.x; i < nh * parts; i += kThreads) w[i] = __ldcg(a.ws_lse + row0 * parts + i);
+        __syncthreads();
+        if (threadIdx.x < nh) {
+            const int h = threadIdx.x;
+            float M = -INFINITY;
+            for (int p = 0; p < parts; ++p) M = fmaxf(M, w[h * parts + p]);
+            float sum = 0.f;
+            for (int p = 0; p < parts; ++p) {
+                const float l = w[h * parts + p];
+                const float wt = (M == -INFINITY || l == -INFINITY) ? 0.f : fast_exp2((l - M) * kLog2e);
+                w[h * parts + p] = wt;  // empty partitions (lse = -inf) weigh 0
+                sum += wt;
             }
+            den[h] = sum;
         }
-        if (lane < kQuads) {
-            const float inv = den > 0.f ? 1.f / den : 0.f;
-            __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + row * D + lane * 4);
+        __syncthreads();
+        // out[h][4q .. 4q+3] = sum_p w[h][p] O_p[h][4q ..] / den[h]: the P loads of an item are
+        // independent of one another, so they are in flight together
+        for (int it = threadIdx.x; it < nh * kQuads; it += kThreads) {
+            const int h = it / kQuads, qd = it % kQuads;
+            const float4* op = reinterpret_cast<const float4*>(a.ws_o + (row0 + h) * parts * D) + qd;
+            const float* wh = w + h * parts;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int p = 0; p < parts; ++p) {
+                const float4 v = __ldcg(op + (size_t)p * kQuads);
+                const float wt = wh[p];
+                acc.x += wt * v.x;
+                acc.y += wt * v.y;
+                acc.z += wt * v.z;
+                acc.w += wt * v.w;
+            }
+            const float inv = den[h] > 0.f ? 1.f / den[h] : 0.f;
+            __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + (row0 + h) * D + qd * 4);
             dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
             dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
         }
@@ -357,7 +367,8 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             a.ws_o[row * D + dd] = den > 0.f ? cta[32 + e] / den : 0.f;
             if (dd == 0) a.ws_lse[row] = den > 0.f ? (cta[h] + log2f(den)) * kLn2 : -INFINITY;
         }
-        if (a.arrivals != nullptr) merge_if_last<D>(a, b, kvh, parts, R);
+        // the merge may reuse the whole data region of shared memory: the partials are written
+        if (a.arrivals != nullptr) merge_if_last<D>(a, b, kvh, parts, R, part, Sh::data_bytes(stages) / 4);
         return;
     }
     // element e = row * D + d of this CTA's output -> its place in out
@@ -433,10 +444,10 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             *reinterpret_cast<__nv_bfloat162*>(dst + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
         }
     }
-    if (SPLIT && a.arrivals != nullptr) __threadfence();  // this CTA's O_p slice, before the count
     cluster.sync();  // keep this CTA's partial alive until every reader is done
-    // the partition is complete once every member has passed the barrier: its rank 0 counts it in
-    if (SPLIT && a.arrivals != nullptr && rank == 0) merge_if_last<D>(a, b, kvh, parts, R);
+    // the partition is complete once every member has passed the barrier (whose release /
+    // acquire orders the members' O_p slices before it): its rank 0 counts it in
+    if (SPLIT && a.arrivals != nullptr && rank == 0) merge_if_last<D>(a, b, kvh, parts, R, part, Sh::data_bytes(stages) / 4);
 }
 
 // out[r, :] = sum_p exp(lse_p - M) O_p / sum_p exp(lse_p - M) with M = max_p lse_p.

@@ -124,6 +124,71 @@ def test_generated_tokens_are_cached_and_eviction_order():
     assert c == 16                                # block 0 survived, block 1 was evicted
 
 
+def test_partial_block_hit_copy_on_write():
+    """A cached prefix that ends inside a block ("Warm Prefix-Cache TTFT": a warm request
+    computes only what its cached prefix does not cover): the leading rows of the cached block
+    that follows the same prefix are copied into the request's own block, never written in
+    place, and the source block is held until the request is released."""
+    rng = np.random.default_rng(7)
+    a = rng.integers(0, 5000, 800).tolist()
+    bm = pa.BlockManager(100)
+    ta, ca, sa, da = bm.admit_cow(1, a, 0)
+    assert ca == 0 and len(sa) == 0 and len(ta) == 50
+    bm.commit(1, [], 800)                         # 50 full blocks enter the cache
+    bm.release(1)
+    assert bm.stats() == (50, 50, 0)
+    b = a[:770] + rng.integers(5000, 9000, 254).tolist()
+    tb, cb, src, dst = bm.admit_cow(2, b, 0)
+    assert cb == 770 and list(tb[:48]) == list(ta[:48]) and tb[48] not in ta
+    assert list(src) == [ta[48] * 16, ta[48] * 16 + 1] and list(dst) == [tb[48] * 16, tb[48] * 16 + 1]
+    # 48 shared + the pinned source (held, idle no more) + 16 own blocks
+    assert bm.stats() == (50 - 16, 50 - 49, 48 + 1 + 16)
+    # the plain admission of the same prompt shares whole blocks only
+    tc, cc = bm.admit(3, b, 0)
+    assert cc == 768 and list(tc[:48]) == list(ta[:48])
+    bm.release(3)
+    bm.release(2)                                 # the pinned source goes back to the idle cache
+    free, idle, used = bm.stats()
+    assert used == 0 and idle >= 50
+    # a divergence at the first token of the block: no partial hit
+    c = a[:768] + [9999] + a[769:790]
+    _, cc, src, _ = bm.admit_cow(4, c, 0)
+    assert cc == 768 and len(src) == 0
+    bm.release(4)
+    # the prompt's last token is always left to compute: 790 tokens match 49 full blocks
+    # (784 tokens) and at most 5 more rows
+    _, cc, src, _ = bm.admit_cow(5, a[:790], 0)
+    assert cc == 789 and len(src) == 5
+    bm.release(5)
+    # the longest matching child wins among several blocks after the same prefix
+    d = a[:784] + a[784:787] + [4242] * 13
+    bm.admit(6, d, 0)
+    bm.commit(6, [], 800)
+    bm.release(6)
+    _, cc, src, _ = bm.admit_cow(7, a[:784] + a[784:794] + [1], 0)
+    assert cc == 794 and list(src) == [int(ta[49]) * 16 + k for k in range(10)]
+
+
+def test_partial_block_hit_admission_counts_the_pinned_block():
+    """Full-lifetime admission counts the held source block: a request that would fit only by
+    evicting that very block is rejected and nothing changes."""
+    a = list(range(1000, 1040))                   # 40 tokens, 3 blocks: blocks 0 and 1 full and cached
+    bm = pa.BlockManager(4)
+    bm.admit_cow(1, a, 0)
+    bm.commit(1, [], 40)
+    bm.release(1)
+    assert bm.stats() == (2, 2, 0)
+    # 20 matching tokens + 40 more: block 0 shared, 4 rows of block 1 copied (it is held), 3 new
+    # blocks needed but only 2 left without evicting the held block: rejected, nothing changes
+    assert bm.admit_cow(2, a[:20] + list(range(5000, 5040)), 0) is None
+    assert bm.stats() == (2, 2, 0)
+    t, cc, src, dst = bm.admit_cow(3, a[:20] + list(range(5000, 5020)), 0)   # 40 tokens: 3 blocks
+    assert cc == 20 and len(src) == 4 and list(t[:1]) == [0]
+    assert bm.stats() == (0, 0, 4)
+    bm.release(3)
+    assert bm.stats()[2] == 0
+
+
 def test_slots_and_errors():
     bm = pa.BlockManager(8)
     t, _ = bm.admit(7, list(range(20)), 12)       # 32 tokens -> 2 blocks

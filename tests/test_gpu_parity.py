@@ -455,6 +455,81 @@ def test_prefix_cache_warm_hit_end_to_end():
     compare(out, ref, "warm prefix hit through the block manager")
 
 
+def test_kv_copy_bit_exact():
+    """pa_kv_copy moves whole pool rows (every kv head, K and V): against the same copies done
+    on the host; skipped pairs (negative slot) and an out-of-pool slot (flagged) copy nothing."""
+    case = W.random_case(6100, batch=4, num_heads=16, num_kv_heads=4, head_dim=128, min_len=100, max_len=300)
+    g = GpuCase(case)
+    k_ref, v_ref = oracle_pool(case)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(6100)
+    nslots = case.num_blocks * 16
+    perm = rng.permutation(nslots)
+    src, dst = perm[:300].astype(np.int64), perm[300:600].astype(np.int64)  # disjoint
+    src[5] = -1
+    dst[7] = nslots + 2
+    pa.pa_kv_copy(g.pool, torch.from_numpy(src).cuda(), torch.from_numpy(dst).cuda())
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    kf = k_ref.reshape(case.num_blocks, case.num_kv_heads, 16, -1)
+    vf = v_ref.reshape(kf.shape)
+    for s_, d_ in zip(src, dst):
+        if s_ < 0 or d_ >= nslots:
+            continue
+        kf[d_ // 16, :, d_ % 16] = kf[s_ // 16, :, s_ % 16]
+        vf[d_ // 16, :, d_ % 16] = vf[s_ // 16, :, s_ % 16]
+    assert np.array_equal(u16(g.k.cpu()), kf) and np.array_equal(u16(g.v.cpu()), vf)
+
+
+def test_prefix_cache_partial_block_hit_end_to_end():
+    """A warm prefix that ends inside a block: a cold request's 800 tokens are appended and
+    released; a warm request whose first 770 tokens match is admitted with 48 shared blocks and
+    the first 2 rows of the 49th copied into its own block (pa_kv_copy, copy on write), appends
+    only its own 254 tokens and runs the chunked prefill of those 254 queries over the 770
+    cached ones.  The pool matches the oracle's pool (the cold append, then the warm request's
+    rows 768-769 and 770-1023 appended by the oracle), and the output the oracle's prefill."""
+    Hq, Hkv, D, nblk = 32, 8, 128, 160
+    gen = torch.Generator().manual_seed(6002)
+    bf = lambda *s: torch.randn(*s, generator=gen).to(torch.bfloat16)
+    bm = pa.BlockManager(nblk)
+    toks_a = torch.randint(0, 5000, (800,), generator=gen).tolist()
+    table_a, cached_a, src, _ = bm.admit_cow(1, toks_a, 0)
+    assert cached_a == 0 and len(src) == 0
+    k_pool = torch.full((nblk, Hkv, 16, D), float("nan"), dtype=torch.bfloat16)
+    v_pool = k_pool.clone()
+    k_np, v_np = u16(k_pool).copy(), u16(v_pool).copy()      # the oracle's own pool
+    kd, vd = k_pool.cuda(), v_pool.cuda()
+    pool = pa.PaPool(kd, vd)
+    orc = oracle.load()
+    k_a, v_a = bf(800, Hkv, D), bf(800, Hkv, D)
+    slots_a = bm.slots(1, 0, 800)
+    pa.pa_kv_append(pool, k_a.cuda(), v_a.cuda(), torch.from_numpy(slots_a).cuda())
+    orc.kv_append(k_np, v_np, u16(k_a), u16(v_a), slots_a)
+    bm.commit(1, [], 800)
+    bm.release(1)
+
+    toks_b = toks_a[:770] + torch.randint(5000, 9000, (254,), generator=gen).tolist()
+    table_b, cached_b, src, dst = bm.admit_cow(2, toks_b, 0)
+    assert cached_b == 770 and list(table_b[:48]) == list(table_a[:48]) and table_b[48] not in table_a
+    assert len(src) == 2
+    pa.pa_kv_copy(pool, torch.from_numpy(src).cuda(), torch.from_numpy(dst).cuda())
+    # the oracle's pool: the warm request's rows 768-769 are the cold request's (same tokens)
+    orc.kv_append(k_np, v_np, u16(k_a[768:770]), u16(v_a[768:770]), bm.slots(2, 768, 2))
+    k_b, v_b = bf(254, Hkv, D), bf(254, Hkv, D)
+    slots_b = bm.slots(2, 770, 254)
+    pa.pa_kv_append(pool, k_b.cuda(), v_b.cuda(), torch.from_numpy(slots_b).cuda())
+    orc.kv_append(k_np, v_np, u16(k_b), u16(v_b), slots_b)
+    q = bf(254, Hq, D)
+    bt = torch.from_numpy(table_b.astype(np.int32)).view(1, -1)
+    sl = torch.tensor([1024], dtype=torch.int32)
+    cu = torch.tensor([0, 254], dtype=torch.int32)
+    scale = 1.0 / math.sqrt(D)
+    out = pa.pa_prefill_chunked(pool, q.cuda(), cu.cuda(), bt.cuda(), sl.cuda(), scale, 254)
+    check_status_clean("partial-block prefix hit")
+    assert np.array_equal(u16(kd.cpu()), k_np) and np.array_equal(u16(vd.cpu()), v_np)
+    ref = orc.prefill(k_np, v_np, u16(q), cu.numpy(), bt.numpy(), sl.numpy(), scale)
+    compare(out, ref, "warm prefix ending inside a block (copy on write)")
+
+
 def test_decode_large_batch_and_pool():
     """2048 sequences (a grid dimension far past the SM count) over a 65536-block pool whose
     block ids run to the end of the pool; decode and the split-KV path."""
