@@ -5,9 +5,9 @@ The metric is paged-GQA decode KV GB/s.  The headline step is one pass of the de
 over their workloads, inputs resident in HBM:
   1. pa_append_decode          append of 64 new tokens fused with the batched decode (64 seqs,
                                ctx ~U[1024,1152], 32q/8kv/128): pa_kv_append + pa_decode in one launch
-  2. pa_decode_splitkv_merged  4 x 8192, P in 8..32, the log-sum-exp merge in the same launch
-                               (Qwen3-32B-shaped 64q/8kv/128)
-  3. pa_decode_splitkv_merged  1 x 32768, P in 8..32
+  2. pa_decode_splitkv         4 x 8192, P in 8..32 (Qwen3-32B-shaped 64q/8kv/128), then
+     pa_combine                its log-sum-exp merge
+  3. pa_decode_splitkv         1 x 32768, P in 8..32, then pa_combine
 value = the KV bytes those calls must read (each (block, kv head) tile once) / step time.
 The full hot path adds the chunked prefill's workload to the step ("full_step"):
   4. pa_kv_append              8 x 256 chunk tokens
@@ -19,11 +19,13 @@ serving loop replays its step.  The same calls one after another on one stream a
 ("step_serial_us").  L2 is flushed (a 512 MB buffer is read) before every timed replay, outside
 the timed interval.
 
-Every call is also timed on its own ("per_call"): a graph of [L2 flush, event, call, event] is
-replayed and the interval between the two event nodes is the call's device time (median, p10,
-p90), so it carries no graph-launch latency; "us_launch" is the same call timed with events
-around the whole replay (launch latency included).  Fractions are given against the measured
-HBM copy peak and the nominal 8 TB/s, or the measured bf16 peak.
+Every call is also timed on its own ("per_call"; the split-KV partitions and their combine as
+one unit): a graph of [L2 flush, event, call, event] is replayed and the interval between the
+two event nodes is "us_isolated" (it carries the call's launch latency: about 5 us even for
+an empty kernel on this harness).  "us" is the marginal cost of one more launch in a stream:
+the same graph with the call run a second time on a second, untouched copy of its inputs
+(L2-cold as well), minus the isolated time (median, p10, p90).  Fractions use "us", against
+the measured HBM copy peak and the nominal 8 TB/s, or the measured bf16 peak.
 
 The end-to-end numbers ("e2e" for the decode step, "full_step.e2e" for the full path) run the
 step through the public API with host buffers, the copies inside the timed interval: each
@@ -64,7 +66,7 @@ import torch  # noqa: E402
 
 METRIC = "paged GQA decode: KV GB/s & frac of GB300 HBM peak; µs/call per batch×ctx"
 WORKLOAD = ("decode step: fused append(64)+decode 64x~1088 (32q/8kv/128) + split-KV 4x8192 and 1x32768 "
-            "(P in 8..32, merged in the launch; 64q/8kv/128); block 16; bf16 N(0,1)")
+            "(P in 8..32) with their log-sum-exp combine (64q/8kv/128); block 16; bf16 N(0,1)")
 FULL_WORKLOAD = WORKLOAD.replace("decode step", "full hot path") + (
     " + append(2048) + chunked prefill 8x256 over a shared 768-token prefix (32q/8kv/128)")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -191,17 +193,26 @@ def attn_bytes(case) -> int:
 
 
 class Call:
-    def __init__(self, name, kind, fn, units, unit_kind, workload):
-        self.name, self.kind, self.fn, self.units, self.unit_kind, self.workload = (name, kind, fn, units, unit_kind,
-                                                                                   workload)
+    """One unit of the step's work as timed on its own: one or more launches of one workload
+    (the split-KV partitions and their merge together), with its algorithmic work."""
+
+    def __init__(self, name, kind, fns, units, unit_kind, workload):
+        self.name, self.kind, self.fns, self.units, self.unit_kind, self.workload = (name, kind, fns, units, unit_kind,
+                                                                                    workload)
+
+    def fn(self):
+        for f in self.fns:
+            f()
 
 
 class Step:
-    """Device-resident inputs of the benchmark's workloads and the calls that make a step."""
+    """Device-resident inputs of the benchmark's workloads and the calls that make a step.
+    With copies=2 every workload also has a second, independent set of device buffers
+    (calls_alt), for timing a call as the marginal cost of one more launch on cold inputs."""
 
     GROUPS = {"decode": ("c3",), "splitkv": ("c4a", "c4b"), "prefill": ("c5",), "decode_step": ("c3", "c4a", "c4b")}
 
-    def __init__(self, device, only=None):
+    def __init__(self, device, only=None, copies=1):
         import paged_kv_gqa_slot_gb300 as pa
         import workloads as W
         self.pa = pa
@@ -213,9 +224,23 @@ class Step:
         self.c5 = W.chunked_prefill() if "c5" in groups else None
         log(f"[bench] workloads drawn in {time.time() - t0:.1f}s")
         self.dev = device
-        d = device
+        # partitions as the library suggests, kept within the workload's 8..32
+        self.P4a = min(32, max(8, pa.pa_splitkv_num_partitions(4, 8, 512))) if self.c4a is not None else 8
+        self.P4b = min(32, max(8, pa.pa_splitkv_num_partitions(1, 8, 2048))) if self.c4b is not None else 32
+        self.copies = [self._upload() for _ in range(copies)]
+        self.calls = self._calls(self.copies[0])
+        self.calls_alt = self._calls(self.copies[1]) if copies > 1 else None
+        g3, g4a, g4b, g5 = (self.copies[0][k] for k in ("c3", "c4a", "c4b", "c5"))
+        self.by_name = {"batched_decode": (g3, self.c3), "splitkv_4x8192": (g4a, self.c4a),
+                        "splitkv_1x32768": (g4b, self.c4b), "chunked_prefill": (g5, self.c5)}
+        self.available = tuple(w for w in FULL_WORKLOADS if self.by_name[w][1] is not None)
+        self.streams = {w: torch.cuda.Stream(device=device) for w in self.available}
 
-        def up(c):
+    def _upload(self):
+        """One set of device buffers for every workload: {"c3": g, ...}."""
+        pa, d = self.pa, self.dev
+
+        def up(c, P=None):
             """A workload's pool, and its per-step inputs packed into one device buffer (views
             at 256-byte aligned offsets, the small tables first, then the new K and V rows and
             q) with a pinned host copy of the same layout: a serving loop stages a step's
@@ -243,51 +268,46 @@ class Step:
             dev.copy_(host)
             g["in_host"], g["in_dev"], g["in_layout"] = host, dev, layout
             g["out"] = torch.empty_like(g["q"])
+            if P is not None:
+                g["ws_o"] = torch.empty((c.batch, c.num_heads, P, c.head_dim), dtype=torch.float32, device=d)
+                g["ws_lse"] = torch.empty((c.batch, c.num_heads, P), dtype=torch.float32, device=d)
             return g
 
-        self.g3, self.g4a, self.g4b, self.g5 = up(self.c3), up(self.c4a), up(self.c4b), up(self.c5)
-        # partitions as the library suggests, kept within the workload's 8..32
-        self.P4a = min(32, max(8, pa.pa_splitkv_num_partitions(4, 8, 512))) if self.c4a is not None else 8
-        self.P4b = min(32, max(8, pa.pa_splitkv_num_partitions(1, 8, 2048))) if self.c4b is not None else 32
-        for g, c, P in ((self.g4a, self.c4a, self.P4a), (self.g4b, self.c4b, self.P4b)):
-            if g is None:
-                continue
-            g["ws_o"] = torch.empty((c.batch, c.num_heads, P, c.head_dim), dtype=torch.float32, device=d)
-            g["ws_lse"] = torch.empty((c.batch, c.num_heads, P), dtype=torch.float32, device=d)
-            g["arrivals"] = torch.zeros(c.batch * c.num_kv_heads, dtype=torch.int32, device=d)
+        return {"c3": up(self.c3), "c4a": up(self.c4a, self.P4a), "c4b": up(self.c4b, self.P4b), "c5": up(self.c5)}
+
+    def _calls(self, gs):
+        pa = self.pa
         c3, c4a, c4b, c5 = self.c3, self.c4a, self.c4b, self.c5
-        g3, g4a, g4b, g5 = self.g3, self.g4a, self.g4b, self.g5
+        g3, g4a, g4b, g5 = gs["c3"], gs["c4a"], gs["c4b"], gs["c5"]
         app_bytes = lambda c: 2 * 2 * c.k_new.numel() * 2  # read new rows, write pool rows, K and V
-        self.calls = []
+        calls = []
         if g3 is not None:
             # the decode step's append and attention in one launch (pa_append_decode)
-            self.calls.append(Call(
+            calls.append(Call(
                 "append_decode[batched_decode,64x~1088]", "decode",
-                lambda: pa.pa_append_decode(g3["pool"], g3["k_new"], g3["v_new"], g3["slots"], g3["q"], g3["bt"],
-                                            g3["sl"], c3.scale, g3["out"]),
+                [lambda: pa.pa_append_decode(g3["pool"], g3["k_new"], g3["v_new"], g3["slots"], g3["q"], g3["bt"],
+                                             g3["sl"], c3.scale, g3["out"])],
                 attn_bytes(c3) + app_bytes(c3), "bytes", "batched_decode"))
         for g, c, P, wl, tag in ((g4a, c4a, self.P4a, "splitkv_4x8192", "4x8192"),
                                  (g4b, c4b, self.P4b, "splitkv_1x32768", "1x32768")):
             if g is None:
                 continue
-            self.calls.append(Call(
-                f"decode_splitkv_merged[{tag},P={P}]", "splitkv",
-                lambda g=g, c=c, P=P: pa.pa_decode_splitkv_merged(g["pool"], g["q"], g["bt"], g["sl"], c.scale, P,
-                                                                  g["ws_o"], g["ws_lse"], g["arrivals"], g["out"]),
+            calls.append(Call(
+                f"decode_splitkv+combine[{tag},P={P}]", "splitkv",
+                [lambda g=g, c=c, P=P: pa.pa_decode_splitkv(g["pool"], g["q"], g["bt"], g["sl"], c.scale, P,
+                                                            g["ws_o"], g["ws_lse"]),
+                 lambda g=g: pa.pa_combine(g["ws_o"], g["ws_lse"], g["out"])],
                 attn_bytes(c), "bytes", wl))
         if g5 is not None:
             mx5 = max(c5.q_lens)
-            self.calls += [
+            calls += [
                 Call("kv_append[chunked_prefill,2048]", "append",
-                     lambda: pa.pa_kv_append(g5["pool"], g5["k_new"], g5["v_new"], g5["slots"]), app_bytes(c5),
+                     [lambda: pa.pa_kv_append(g5["pool"], g5["k_new"], g5["v_new"], g5["slots"])], app_bytes(c5),
                      "bytes", "chunked_prefill"),
                 Call("prefill_chunked[8x256 over 768]", "prefill",
-                     lambda: pa.pa_prefill_chunked(g5["pool"], g5["q"], g5["cu"], g5["bt"], g5["sl"], c5.scale, mx5,
-                                                   g5["out"]), causal_flops(c5), "flops", "chunked_prefill")]
-        self.by_name = {"batched_decode": (g3, c3), "splitkv_4x8192": (g4a, c4a), "splitkv_1x32768": (g4b, c4b),
-                        "chunked_prefill": (g5, c5)}
-        self.available = tuple(w for w in FULL_WORKLOADS if self.by_name[w][1] is not None)
-        self.streams = {w: torch.cuda.Stream(device=d) for w in self.available}
+                     [lambda: pa.pa_prefill_chunked(g5["pool"], g5["q"], g5["cu"], g5["bt"], g5["sl"], c5.scale, mx5,
+                                                    g5["out"])], causal_flops(c5), "flops", "chunked_prefill")]
+        return calls
 
     def kv_bytes(self, workloads) -> int:
         """KV bytes the attention calls of these workloads must read (unique rows)."""
@@ -295,6 +315,9 @@ class Step:
 
     def calls_of(self, workloads):
         return [c for c in self.calls if c.workload in workloads]
+
+    def launches(self, workloads) -> int:
+        return sum(len(c.fns) for c in self.calls_of(workloads))
 
     def run(self, workloads):
         """The workloads' calls one after another on the current stream."""
@@ -353,7 +376,7 @@ class E2E:
             g, c = step.by_name[w]
             if w != "chunked_prefill":
                 d2h = [(torch.empty_like(g["out"], device="cpu").pin_memory(), g["out"])]
-                fns = [call.fn for call in step.calls_of((w,))]
+                fns = [f for call in step.calls_of((w,)) for f in call.fns]
                 self.pieces.append(([(g["in_host"], g["in_dev"])], d2h, fns, w))
                 continue
             assert c.k_new.shape[0] == sum(c.q_lens), "prefill workload: one appended row per chunk query"
@@ -520,15 +543,27 @@ def time_step(step, workloads, steps, warmup, flush_buf, dev, serial=False):
 
 
 def time_calls(step, steps, flush_buf, dev):
-    """Every call of the step on its own: in-graph event interval and the with-launch time."""
+    """Every call unit of the step on its own, L2 cold: (marginal, isolated) device times (us).
+    isolated: the unit alone after an L2 flush, between event nodes of one graph (it carries
+    the unit's launch latency, about 5 us on this harness even for an empty kernel).
+    marginal: what one more launch of the unit costs in a stream -- the same graph with the
+    unit run a second time on the second, untouched copy of its inputs, minus the isolated
+    graph; the second launch's start overlaps the first one's tail, as in a serving loop."""
     res = {}
-    for c in step.calls:
-        kern = time_in_graph(c.fn, steps, flush_buf, dev)
-        g1 = capture_graph(c.fn, dev)
-        time_graph(g1, 2, flush_buf)
-        launch = time_graph(g1, steps, flush_buf)
-        del g1
-        res[c.name] = (kern if kern is not None else launch, launch)
+    for c, c2 in zip(step.calls, step.calls_alt or step.calls):
+        one = time_in_graph(c.fn, steps, flush_buf, dev)
+        if one is None:  # no event nodes in graphs: whole-replay timing
+            g1 = capture_graph(c.fn, dev)
+            time_graph(g1, 2, flush_buf)
+            one = time_graph(g1, steps, flush_buf)
+            del g1
+            res[c.name] = (one, one)
+            continue
+        if step.calls_alt is None:
+            res[c.name] = (one, one)
+            continue
+        two = time_in_graph(lambda: (c.fn(), c2.fn()), steps, flush_buf, dev)
+        res[c.name] = (two - np.median(one), one)
     return res
 
 
@@ -786,11 +821,11 @@ def run_reference(args, ws, rank):
 
 
 def call_entry(call, kern_us, launch_us, peaks, peak_src):
-    """Per-call record: in-graph device time (median, p10, p90), the same with the graph
-    launch, and the achieved rate against the peaks."""
+    """Per-call record: marginal device time in a stream (median, p10, p90), the isolated
+    time with its launch latency, and the achieved rate against the peaks."""
     st = stats(kern_us)
     med = st["median"]
-    e = {"us": st, "us_launch": stats(launch_us)}
+    e = {"launches": len(call.fns), "us": st, "us_isolated": stats(launch_us)}
     if call.unit_kind == "bytes":
         gbs = call.units / med / 1e3
         e.update({"bytes": int(call.units), "GB/s": round(gbs, 1), **hbm_fracs(gbs, peaks)})
@@ -844,7 +879,7 @@ def main(argv=None):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     peaks, peak_src = load_peaks()
-    step = Step(dev, args.only)
+    step = Step(dev, args.only, copies=2)
     extras = args.only is None
     headline = tuple(w for w in DECODE_WORKLOADS if w in step.available) or step.available
     full = step.available
@@ -934,7 +969,7 @@ def main(argv=None):
             ("step_parallel_us" if args.serial_step else "step_serial_us"): stats(other_us),
             "full_step": full_step, "roofline": roof, "rooflines": rooflines, "per_call": calls, "latency": lat,
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": len(head_calls) * args.steps, "clocks": clocks,
+            "gpu_launches": step.launches(headline) * args.steps, "clocks": clocks,
             "wall_s_timed": round(wall, 3),
         }
         print(json.dumps(line), flush=True)

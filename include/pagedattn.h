@@ -27,7 +27,7 @@
  *   pool K, V      [num_blocks, num_kv_heads, 16, head_dim]   bf16, 16-byte aligned
  *   slot           block_id * 16 + offset_in_block
  *   block_tables   [batch, max_blocks] int32; entries past ceil(seq_len / 16) never affect
- *                  a result (a decode may load the first min(32, max_blocks) entries of a row
+ *                  a result (a decode may load up to 32 entries of a row, all within the row,
  *                  before it knows seq_len, and ignores those it does not need)
  *   seq_lens       [batch] int32, tokens in the sequence including any appended this step
  *   q, out         decode [batch, num_heads, head_dim]; prefill [sum of chunk lengths,
@@ -162,28 +162,6 @@ int pa_decode_splitkv(const pa_pool *pool, const void *q, const int32_t *block_t
                       int32_t num_partitions, float *ws_o, float *ws_lse, pa_stream_t stream);
 
 /*
- * pa_decode_splitkv_merged -- pa_decode_splitkv followed by pa_combine, in one launch.  The
- * partitions are the same and write ws_o / ws_lse as pa_decode_splitkv does; then every
- * partition of a (sequence, kv head) counts itself in on that pair's arrival counter, and the
- * partition that arrives last (none waits for another) merges all P of them into out as
- * pa_combine would.
- *   ws_o, ws_lse   as pa_decode_splitkv (scratch owned by the caller; both are read back)
- *   arrivals       [batch * num_kv_heads] uint32, device memory owned by the caller.  It must
- *                  hold zeros before the first call (e.g. cudaMemset once at allocation); every
- *                  call sets each counter it used back to zero, so it needs no clearing between
- *                  calls.  A counter found non-zero at entry sets PA_DEV_OUT_OF_RANGE (its
- *                  sequence's output is then not written); after a call that ended with
- *                  PA_DEV_TIMEOUT, zero the counters again.  Calls that may run at the same time
- *                  need their own ws_o / ws_lse / arrivals.
- *   out            [batch, num_heads, head_dim] bf16
- * Other arguments and errors as pa_decode_splitkv.
- */
-int pa_decode_splitkv_merged(const pa_pool *pool, const void *q, const int32_t *block_tables, int32_t max_blocks,
-                             const int32_t *seq_lens, int32_t batch, int32_t num_heads, float scale,
-                             int32_t num_partitions, float *ws_o, float *ws_lse, uint32_t *arrivals, void *out,
-                             pa_stream_t stream);
-
-/*
  * pa_combine -- log-sum-exp merge of split-KV partitions:
  *   M = max_p lse_p;  w_p = exp(lse_p - M);  out = sum_p w_p O_p / sum_p w_p
  * (partitions with lse_p = -inf weigh 0; all empty gives a zero row).
@@ -248,9 +226,10 @@ size_t pa_noalloc_scratch_bytes(void);
 int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
 
 /*
- * Partition count suggested for pa_decode_splitkv on the current device (1..64): the
- * largest count whose CTAs (batch x num_kv_heads x count) fit one wave of four per SM,
- * keeping >= 8 blocks per partition.
+ * Partition count suggested for pa_decode_splitkv on the current device (1..16): the
+ * largest power of two, at most 16, whose CTAs (batch x num_kv_heads x count) fit one wave
+ * of four per SM, keeping >= 8 blocks per partition (the library runs each partition on a
+ * thread-block cluster of up to 4 CTAs when the partitions alone leave the wave short).
  */
 int pa_splitkv_num_partitions(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
 

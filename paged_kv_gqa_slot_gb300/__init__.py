@@ -20,7 +20,7 @@ from typing import Optional, Tuple
 
 import torch
 
-__all__ = ["PaPool", "pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decode", "pa_decode_splitkv", "pa_decode_splitkv_merged",
+__all__ = ["PaPool", "pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decode", "pa_decode_splitkv",
            "pa_combine", "pa_prefill_chunked",
            "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "pa_splitkv_num_partitions",
            "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes", "PagedAttnError",
@@ -30,8 +30,8 @@ __all__ = ["PaPool", "pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decod
 BLOCK_SIZE = 16
 PKG = Path(__file__).resolve().parent
 _LIB_PATH = PKG / "libpagedattn.so"
-EXPORTED_SYMBOLS = ("pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decode", "pa_splitkv_workspace_bytes", "pa_decode_splitkv",
-                    "pa_decode_splitkv_merged", "pa_combine",
+EXPORTED_SYMBOLS = ("pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decode", "pa_splitkv_workspace_bytes",
+                    "pa_decode_splitkv", "pa_combine",
                     "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_splitkv_num_partitions",
                     "pa_status_str", "pa_version", "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes",
                     "pa_kv_block_bytes", "pa_kv_budget_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_admit", "pa_bm_admit_cow",
@@ -85,7 +85,6 @@ def library() -> ctypes.CDLL:
         "pa_append_decode": (ctypes.c_int, [pool, P, P, P, P, P, I32, P, I32, I32, F32, P, P]),
         "pa_splitkv_workspace_bytes": (SZ, [I32, I32, I32, I32]),
         "pa_decode_splitkv": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, I32, P, P, P]),
-        "pa_decode_splitkv_merged": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, I32, P, P, P, P, P]),
         "pa_combine": (ctypes.c_int, [P, P, I32, I32, I32, I32, P, P]),
         "pa_prefill_chunked": (ctypes.c_int, [pool, P, P, P, I32, P, I32, I32, I32, F32, P, P]),
         "pa_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32, P]),
@@ -260,32 +259,6 @@ def pa_decode_splitkv(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor,
                                      _stream(stream))
     _check(rc, "pa_decode_splitkv")
     return ws_o, ws_lse
-
-
-def pa_decode_splitkv_merged(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
-                             scale: float, num_partitions: int, ws_o: torch.Tensor, ws_lse: torch.Tensor,
-                             arrivals: torch.Tensor, out: Optional[torch.Tensor] = None,
-                             stream=None) -> torch.Tensor:
-    """pa_decode_splitkv and pa_combine in one launch.  `arrivals` is an int32 tensor of
-    batch * num_kv_heads counters that must be zero before the first call (every call leaves
-    it zero)."""
-    B, Hq, D = q.shape
-    _tables(block_tables, seq_lens, B)
-    P = int(num_partitions)
-    if tuple(ws_o.shape) != (B, Hq, P, D) or tuple(ws_lse.shape) != (B, Hq, P):
-        raise ValueError(f"ws_o / ws_lse: need shapes {(B, Hq, P, D)} / {(B, Hq, P)}, "
-                         f"got {tuple(ws_o.shape)} / {tuple(ws_lse.shape)}")
-    if arrivals.numel() != B * pool.num_kv_heads:
-        raise ValueError(f"arrivals: need {B * pool.num_kv_heads} counters, got {arrivals.numel()}")
-    out = _out(out, q.shape, q)
-    rc = library().pa_decode_splitkv_merged(pool.ref, _dev(q, torch.bfloat16, "q"),
-                                            _dev(block_tables, torch.int32, "block_tables"), block_tables.shape[1],
-                                            _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, float(scale), P,
-                                            _dev(ws_o, torch.float32, "ws_o"), _dev(ws_lse, torch.float32, "ws_lse"),
-                                            _dev(arrivals, torch.int32, "arrivals"), _dev(out, torch.bfloat16, "out"),
-                                            _stream(stream))
-    _check(rc, "pa_decode_splitkv_merged")
-    return out
 
 
 def pa_decode_splitkv_noalloc(pool: PaPool, q: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,

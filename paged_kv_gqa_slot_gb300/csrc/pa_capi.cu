@@ -44,17 +44,22 @@ struct MapKey {
     const void* base;
     long long rows;
     int d;
-    int kind;  // 0: 2-D half-tile boxes, 1: 4-D whole-tile boxes
+    int kind;   // 0: 2-D half-tile boxes, 1: 4-D whole-tile boxes, 2: 3-D (d, head, token) rows
+    int extra;  // kind 2: heads * 65536 + box heads
     bool operator==(const MapKey& o) const {
-        return base == o.base && rows == o.rows && d == o.d && kind == o.kind;
+        return base == o.base && rows == o.rows && d == o.d && kind == o.kind && extra == o.extra;
     }
 };
 struct MapKeyHash {
     size_t operator()(const MapKey& k) const {
         return std::hash<const void*>()(k.base) ^ (std::hash<long long>()(k.rows) * 31u) ^ (size_t)k.d ^
-               ((size_t)k.kind << 20);
+               ((size_t)k.kind << 20) ^ ((size_t)k.extra << 24);
     }
 };
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash>& map_cache() {
+    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
+    return cache;
+}
 
 // TMA maps over one pool tensor, 128-byte swizzled (see PoolView).  A map depends only on
 // (address, rows, head_dim, kind), so cached maps never go stale.
@@ -62,8 +67,8 @@ struct MapKeyHash {
 //   kind 1: (64, 16, head_dim/64, rows/16) with strides (2*head_dim, 128, 32*head_dim) bytes,
 //           box (64, 16, head_dim/64, 1): a whole (block, head) tile landing half-major.
 bool pool_map(CUtensorMap* out, void* base, long long rows, int d, int kind) {
-    static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> cache;
-    const MapKey key{base, rows, d, kind};
+    auto& cache = map_cache();
+    const MapKey key{base, rows, d, kind, 0};
     {
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = cache.find(key);
@@ -132,6 +137,41 @@ int check_heads(const PoolView& v, int num_heads) {
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
 }  // namespace
+
+// 3-D map (d, head, token) over a [tokens, heads, d] bf16 tensor, 128-byte swizzled, whose
+// box is (64 columns, box_heads heads, box_tokens tokens): one column half of a query tile
+// whose rows are (token, head) pairs.  Cached like the pool maps.
+bool rows_map(CUtensorMap* out, const void* base, long long tokens, int heads, int d, int box_heads, int box_tokens) {
+    if (tokens <= 0 || heads <= 0 || d != 128 || box_heads <= 0 || box_heads > 256 || box_tokens <= 0 ||
+        box_tokens > 256 || box_heads > heads)
+        return false;
+    auto& cache = map_cache();
+    const MapKey key{base, tokens, d, 2, heads * 65536 + box_heads};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) {
+            *out = it->second;
+            return true;
+        }
+    }
+    auto fn = encode_fn();
+    if (!fn) return false;
+    CUtensorMap m;
+    const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)tokens};
+    const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+    const cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_tokens};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (cache.size() > 256) cache.clear();
+    cache[key] = m;
+    *out = m;
+    return true;
+}
 
 const DeviceInfo& device_info() {
     static DeviceInfo infos[kMaxDevices];
@@ -289,37 +329,6 @@ int pa_decode_splitkv(const pa_pool* pool, const void* q, const int32_t* block_t
     a.seq_lens = seq_lens;
     a.ws_o = ws_o;
     a.ws_lse = ws_lse;
-    a.status = device_status_ptr();
-    if (!a.status) return PA_ERR_CUDA;
-    a.batch = batch;
-    a.num_heads = num_heads;
-    a.max_blocks = max_blocks;
-    a.num_partitions = num_partitions;
-    a.scale = scale;
-    return from_cuda(launch_decode_splitkv(v, a, (cudaStream_t)stream));
-}
-
-int pa_decode_splitkv_merged(const pa_pool* pool, const void* q, const int32_t* block_tables, int32_t max_blocks,
-                             const int32_t* seq_lens, int32_t batch, int32_t num_heads, float scale,
-                             int32_t num_partitions, float* ws_o, float* ws_lse, uint32_t* arrivals, void* out,
-                             pa_stream_t stream) {
-    PoolView v;
-    int rc = check_attn(pool, &v, q, block_tables, max_blocks, seq_lens, batch, num_heads, scale, out);
-    if (rc) return rc;
-    if (num_partitions < 1 || num_partitions > 4096) return PA_ERR_INVALID_ARG;
-    if (batch == 0) return PA_OK;
-    if (!ws_o || !ws_lse || !arrivals || !aligned16(ws_o)) return PA_ERR_INVALID_ARG;
-    if (num_heads / v.num_kv_heads > 16) return PA_ERR_UNSUPPORTED;
-    rc = check_pool(pool, &v, true);
-    if (rc) return rc;
-    AttnArgs a{};
-    a.q = q;
-    a.block_tables = block_tables;
-    a.seq_lens = seq_lens;
-    a.out = out;
-    a.ws_o = ws_o;
-    a.ws_lse = ws_lse;
-    a.arrivals = arrivals;
     a.status = device_status_ptr();
     if (!a.status) return PA_ERR_CUDA;
     a.batch = batch;

@@ -15,11 +15,7 @@
 //     cluster and merges their partials through distributed shared memory (no
 //     workspace, one launch) -- used when batch x kv heads is too small to fill the GPU;
 //   * pa_decode_splitkv writes each partition's normalised O_p and lse_p to the caller's
-//     workspace for pa_combine;
-//   * pa_decode_splitkv_merged does the same and then merges in the same launch: every
-//     partition (CTA, or cluster) of a (sequence, kv head) counts itself in on an arrival
-//     counter once its results are written, and the one that arrives last -- it never waits
-//     for the others -- reads all P partitions back and writes the bf16 output.
+//     workspace for pa_combine.
 #include <algorithm>
 #include <atomic>
 #include <cstdlib>
@@ -77,82 +73,7 @@ struct DecodeArgs {
     const int32_t* cu_q_lens;  // multi-query: chunk of query tokens of each sequence [B+1]
     void* k_pool;  // the pool, for the fused append's row write
     void* v_pool;
-    unsigned* arrivals;  // split-KV merged in the launch: [B * Hkv] counters (zero between calls), or null
 };
-
-// Split-KV merged in the launch.  Called by every thread of the CTA that completed one
-// partition of (sequence b, kv head kvh) after its results are in ws_o / ws_lse (and, for a
-// cluster, after the barrier that follows every member's writes): the CTA counts itself in on
-// the (b, kvh) arrival counter with one acquire-release atomic, and the one that arrives last
-// (no CTA ever waits) reads the P partitions back from L2 and writes the merged bf16 output of
-// the group's heads:
-//   M = max_p lse_p,  w_p = e^{lse_p - M},  out = sum_p w_p O_p / sum_p w_p.
-// The last arrival sets the counter back to zero for the next call.  `scratch` is `room`
-// floats (>= parts + 1) of this CTA's shared memory that nothing else uses any more.
-template <int D>
-__device__ __forceinline__ void merge_if_last(const DecodeArgs& a, int b, int kvh, int parts, int R, float* scratch,
-                                              int room) {
-    __shared__ unsigned s_last;
-    __syncthreads();  // every write of this CTA's partition happens before thread 0's release
-    if (threadIdx.x == 0) {
-        unsigned* cnt = a.arrivals + (size_t)b * a.num_kv_heads + kvh;
-        unsigned prev;
-        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(cnt) : "memory");
-        if (prev >= (unsigned)parts) atomicOr(a.status, kDevOutOfRange);  // counter was not zero at entry
-        const bool last = prev == (unsigned)parts - 1;
-        if (last) atomicExch(cnt, 0u);
-        s_last = last ? 1u : 0u;
-    }
-    __syncthreads();  // thread 0's acquire orders the other partitions' results before our reads
-    if (!s_last) return;
-    constexpr int kQuads = D / 4;
-    // heads per pass: their weights [hp][parts] and sums [hp] fit the scratch
-    const int hp = max(1, min(R, room / (parts + 1)));
-    for (int h0 = 0; h0 < R; h0 += hp) {
-        const int nh = min(hp, R - h0);
-        const size_t row0 = (size_t)b * a.num_heads + (size_t)kvh * a.group + h0;
-        float* w = scratch;                 // [nh][parts]: lse, then the merge weights
-        float* den = scratch + nh * parts;  // [nh]
-        __syncthreads();  // the previous pass is done with the scratch
-        for (int i = threadIdx.x; i < nh * parts; i += kThreads) w[i] = __ldcg(a.ws_lse + row0 * parts + i);
-        __syncthreads();
-        if (threadIdx.x < nh) {
-            const int h = threadIdx.x;
-            float M = -INFINITY;
-            for (int p = 0; p < parts; ++p) M = fmaxf(M, w[h * parts + p]);
-            float sum = 0.f;
-            for (int p = 0; p < parts; ++p) {
-                const float l = w[h * parts + p];
-                const float wt = (M == -INFINITY || l == -INFINITY) ? 0.f : fast_exp2((l - M) * kLog2e);
-                w[h * parts + p] = wt;  // empty partitions (lse = -inf) weigh 0
-                sum += wt;
-            }
-            den[h] = sum;
-        }
-        __syncthreads();
-        // out[h][4q .. 4q+3] = sum_p w[h][p] O_p[h][4q ..] / den[h]: the P loads of an item are
-        // independent of one another, so they are in flight together
-        for (int it = threadIdx.x; it < nh * kQuads; it += kThreads) {
-            const int h = it / kQuads, qd = it % kQuads;
-            const float4* op = reinterpret_cast<const float4*>(a.ws_o + (row0 + h) * parts * D) + qd;
-            const float* wh = w + h * parts;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int p = 0; p < parts; ++p) {
-                const float4 v = __ldcg(op + (size_t)p * kQuads);
-                const float wt = wh[p];
-                acc.x += wt * v.x;
-                acc.y += wt * v.y;
-                acc.z += wt * v.z;
-                acc.w += wt * v.w;
-            }
-            const float inv = den[h] > 0.f ? 1.f / den[h] : 0.f;
-            __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(a.out + (row0 + h) * D + qd * 4);
-            dst[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-            dst[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-        }
-    }
-}
 
 template <int D, int NT, bool SPLIT, bool MQ>
 __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -176,13 +97,23 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = a.group;
     pdl_wait();
-    // A CTA that alone covers its sequence (no partitions, no cluster) starts at block 0: its
-    // producer loads the first 32 table entries now, in parallel with seq_lens, instead of
-    // after it, which takes one dependent memory round trip off the first copy.
+    // The producer loads its first 32 table entries now, in parallel with seq_lens, instead of
+    // after it, which takes one dependent memory round trip off the first copy.  A CTA that
+    // alone covers its sequence starts at block 0; a partition or cluster member's first block
+    // depends on the length, so it guesses the length that fills the table (the common case of
+    // a long context) and keeps the guess only if it gives the same first block.
     const bool whole = parts == 1 && sub == 1;
-    int first_entry = 0;
-    if (whole && warp == kConsumerWarps && lane < a.max_blocks)
-        first_entry = __ldg(a.block_tables + (size_t)b * a.max_blocks + lane);
+    int first_entry = 0, guess0 = 0;
+    if (warp == kConsumerWarps) {
+        if (!whole) {
+            const int nb_g = a.max_blocks;
+            const int per_ug = (nb_g + parts - 1) / parts;
+            const int nu_g = max(0, min(per_ug, nb_g - unit * per_ug));
+            const int per_g = (nu_g + sub - 1) / sub;
+            guess0 = unit * per_ug + sub_rank * per_g;
+        }
+        if (guess0 + lane < a.max_blocks) first_entry = __ldg(a.block_tables + (size_t)b * a.max_blocks + guess0 + lane);
+    }
 
     int L = a.seq_lens[b];
     if (L < 0 || L > a.max_blocks * kBlockSize) {
@@ -262,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         }
         produce_kv_blocks<D>(smem, stages, full, empty, &tm_k, &tm_v,
                              a.block_tables + (size_t)b * a.max_blocks + blk0, n, a.num_blocks, a.num_kv_heads, kvh,
-                             a.status, l2_evict_first_policy(), first_entry, whole && blk0 == 0);
+                             a.status, l2_evict_first_policy(), first_entry, blk0 == guess0);
     } else {
         uint32_t qb[NT][D / 16][2];
         int colpos[NT][2];  // MQ: causal limit of this thread's two columns per n-tile
@@ -367,8 +298,6 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             a.ws_o[row * D + dd] = den > 0.f ? cta[32 + e] / den : 0.f;
             if (dd == 0) a.ws_lse[row] = den > 0.f ? (cta[h] + log2f(den)) * kLn2 : -INFINITY;
         }
-        // the merge may reuse the whole data region of shared memory: the partials are written
-        if (a.arrivals != nullptr) merge_if_last<D>(a, b, kvh, parts, R, part, Sh::data_bytes(stages) / 4);
         return;
     }
     // element e = row * D + d of this CTA's output -> its place in out
@@ -445,9 +374,6 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
         }
     }
     cluster.sync();  // keep this CTA's partial alive until every reader is done
-    // the partition is complete once every member has passed the barrier (whose release /
-    // acquire orders the members' O_p slices before it): its rank 0 counts it in
-    if (SPLIT && a.arrivals != nullptr && rank == 0) merge_if_last<D>(a, b, kvh, parts, R, part, Sh::data_bytes(stages) / 4);
 }
 
 // out[r, :] = sum_p exp(lse_p - M) O_p / sum_p exp(lse_p - M) with M = max_p lse_p.
@@ -576,7 +502,6 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int grid_x, int 
     da.k_pool = pool.k;
     da.v_pool = pool.v;
     da.cu_q_lens = MQ ? a.cu_q_lens : nullptr;
-    da.arrivals = SPLIT ? a.arrivals : nullptr;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid_x, pool.num_kv_heads, a.batch);
@@ -656,13 +581,18 @@ int decode_splits_for(int batch, int num_kv_heads, int max_blocks) {
 }
 
 int splitkv_partitions_for(int batch, int num_kv_heads, int max_blocks) {
-    // The partitions of all (sequence, kv head) pairs fill one wave of four CTAs per SM as
-    // evenly as possible (an SM holding one CTA more than its neighbours finishes last),
-    // keeping >= 8 blocks per partition; at most 64.
+    // CTAs per (sequence, kv head) pair: the largest power of two whose CTAs fit one wave of
+    // four per SM; the partitions are that many up to 16, and a thread-block cluster per
+    // partition takes the rest (splitkv_cluster_for).  Measured on GB300 (152 SMs, 134 MB of
+    // KV): 4 x 8192 over 8 kv heads runs 27.2 us at P = 16 (512 CTAs) against 28.7 us at
+    // P = 19 (608); 1 x 32768 runs 27.0 us at P = 16 with 4-CTA clusters against 28.7 us at
+    // P = 32 with 2-CTA clusters and 40.6 us at P = 19 with 4-CTA clusters (608 CTAs, which
+    // do not all fit as clusters at once).  At least 8 blocks per partition.
     const int items = std::max(1, batch * num_kv_heads);
-    int p = std::max(1, (4 * device_info().num_sms) / items);
-    p = std::min(p, 64);
-    while (p > 1 && max_blocks / p < 8) --p;
+    const int fit = std::max(1, (4 * device_info().num_sms) / items);
+    int p = 1;
+    while (p * 2 <= fit && p * 2 <= 16) p *= 2;
+    while (p > 1 && max_blocks / p < 8) p /= 2;
     return p;
 }
 
@@ -695,6 +625,8 @@ int splitkv_cluster_for(int batch, int num_kv_heads, int num_partitions, int max
     const long long ctas = (long long)std::max(1, batch) * num_kv_heads * num_partitions;
     int c = forced > 0 ? forced : (int)std::min<long long>(4, (4LL * device_info().num_sms) / ctas);
     c = std::max(1, std::min(c, 8));
+    if (forced <= 0)
+        while (c & (c - 1)) --c;  // a power of two: clusters of 3 place worse than of 2 or 4
     while (c > 1 && max_blocks / ((long long)num_partitions * c) < 4) --c;  // >= ~4 blocks per CTA
     return c;
 }

@@ -57,12 +57,12 @@ struct AttnArgs {
     const void* k_new;
     const void* v_new;
     const int64_t* slots;
-    // split-KV only, merged in the launch (null: partials only, for pa_combine): one arrival
-    // counter per (sequence, kv head), zero between calls
-    unsigned* arrivals;
 };
 
 const DeviceInfo& device_info();
+// 3-D TMA map (d, head, token) over a [tokens, heads, d] bf16 tensor (d = 128), 128-byte
+// swizzled, box (64, box_heads, box_tokens); false if it cannot be encoded.
+bool rows_map(CUtensorMap* out, const void* base, long long tokens, int heads, int d, int box_heads, int box_tokens);
 unsigned* device_status_ptr();
 
 // One-time set-up of a kernel (function attributes, occupancy queries) on each device:
@@ -121,6 +121,8 @@ cudaError_t launch_prefill(const PoolView& pool, const AttnArgs& a, cudaStream_t
 // tcgen05 chunked prefill: head_dim 128 and a group size dividing 128
 bool prefill_tc_supported(int head_dim, int group);
 cudaError_t launch_prefill_tc(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
+// the same shapes, 128-key stages with P in tensor memory
+cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);
 
 // Split count the decode launcher picks for a problem (exposed for tests and tuning).
 int decode_splits_for(int batch, int num_kv_heads, int max_blocks);

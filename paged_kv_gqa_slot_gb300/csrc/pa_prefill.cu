@@ -195,13 +195,16 @@ cudaError_t launch_prefill(const PoolView& pool, const AttnArgs& a, cudaStream_t
     // A chunk of a few queries (a speculative-decoding verify, one decode token) is a
     // bandwidth-bound decode with a causal mask: it runs on the decode kernel, its
     // (query, head) rows on the MMA N dimension.  PA_PREFILL_IMPL=t or m forces the
-    // tensor-core or warp-MMA prefill kernels instead, for A/B comparisons.
+    // tensor-core or warp-MMA prefill kernels instead, for A/B comparisons; 2 selects the
+    // tensor-core kernel with 128-key stages.
     static const char forced = [] {
         const char* e = std::getenv("PA_PREFILL_IMPL");
         return e ? e[0] : '\0';
     }();
-    if (forced != 't' && forced != 'm' && decode_mq_supported(g, a.max_chunk)) return launch_decode_mq(pool, a, stream);
-    if (prefill_tc_supported(pool.head_dim, g)) return launch_prefill_tc(pool, a, stream);
+    if (forced != 't' && forced != 'm' && forced != '2' && decode_mq_supported(g, a.max_chunk))
+        return launch_decode_mq(pool, a, stream);
+    if (prefill_tc_supported(pool.head_dim, g))
+        return forced == '2' ? launch_prefill_tc2(pool, a, stream) : launch_prefill_tc(pool, a, stream);
     if (pool.head_dim == 128) return launch_mma<128>(pool, a, stream);
     return launch_mma<64>(pool, a, stream);
 }

@@ -152,14 +152,16 @@ def _check_split(case, P, pool=None):
 
 @pytest.mark.parametrize("P", [8, 16, 19, 32])
 def test_splitkv_4x8192(P):
-    """P = 19 is the count the library suggests for 4 sequences x 8 kv heads on 152 SMs (one
-    full wave of four CTAs per SM), the one the benchmark runs."""
+    """P = 16 is the count the library suggests for 4 sequences x 8 kv heads on 152 SMs, the
+    one the benchmark runs; 19 fills one wave of four CTAs per SM exactly."""
     case = W.splitkv_decode(1004, 4, 8192)
     _check_split(case, P)
 
 
-@pytest.mark.parametrize("P", [8, 32])
+@pytest.mark.parametrize("P", [8, 16, 32])
 def test_splitkv_1x32768(P):
+    """P = 16 is the count the library suggests for 1 sequence x 8 kv heads (each partition
+    on a 4-CTA cluster), the one the benchmark runs."""
     case = W.splitkv_decode(1004, 1, 32768)
     _check_split(case, P)
 
@@ -168,73 +170,6 @@ def test_splitkv_1x32768(P):
 def test_splitkv_ragged_and_empty_partitions(P):
     case = W.random_case(4000 + P, batch=6, num_heads=16, num_kv_heads=2, head_dim=128, min_len=1, max_len=300)
     _check_split(case, P)
-
-
-def _check_merged(case, P, calls=2):
-    """pa_decode_splitkv_merged against the oracle's decode, `calls` times in a row on the same
-    counters (each call must leave them zero), and its partials against the oracle's."""
-    g = GpuCase(case)
-    B, Hq, D = case.q.shape
-    ws_o = torch.empty((B, Hq, P, D), dtype=torch.float32, device="cuda")
-    ws_lse = torch.empty((B, Hq, P), dtype=torch.float32, device="cuda")
-    arrivals = torch.zeros(B * case.num_kv_heads, dtype=torch.int32, device="cuda")
-    k, v = oracle_pool(case)
-    orc = oracle.load()
-    ref = orc.decode(k, v, u16(case.q), case.block_tables.numpy(), case.seq_lens.numpy(), case.scale)
-    for call in range(calls):
-        out = torch.full_like(g.q, float("nan"))
-        pa.pa_decode_splitkv_merged(g.pool, g.q, g.bt, g.sl, case.scale, P, ws_o, ws_lse, arrivals, out)
-        check_status_clean(f"merged split P={P}, call {call}")
-        compare(out, ref, f"{case.name} P={P} merged in the launch, call {call}")
-        assert int(arrivals.abs().sum()) == 0, "arrival counters not back to zero"
-    o_ref, lse_ref = orc.decode_partitions(k, v, u16(case.q), case.block_tables.numpy(), case.seq_lens.numpy(),
-                                           case.scale, P)
-    fin = np.isfinite(lse_ref)
-    assert np.array_equal(np.isfinite(ws_lse.cpu().numpy()), fin)
-    compare(ws_o[torch.from_numpy(fin).to(ws_o.device)], o_ref[fin], f"{case.name} P={P} merged: partial O")
-    return out
-
-
-@pytest.mark.parametrize("P", [8, 19, 32])
-def test_splitkv_merged_4x8192(P):
-    _check_merged(W.splitkv_decode(1004, 4, 8192), P)
-
-
-@pytest.mark.parametrize("P", [8, 32])
-def test_splitkv_merged_1x32768(P):
-    """Few (sequence, kv head) pairs: each partition runs on a cluster of CTAs whose rank 0
-    counts the partition in once the whole cluster has written it."""
-    _check_merged(W.splitkv_decode(1004, 1, 32768), P)
-
-
-@pytest.mark.parametrize("P", [1, 3, 64])
-def test_splitkv_merged_ragged_and_empty(P):
-    """Ragged lengths (partitions past a short sequence are empty) and a zero-length
-    sequence, whose output row must be zero."""
-    case = W.paged_case(name="merged_ragged", seed=4300 + P, seq_lens=[1, 300, 0, 77, 1000, 16],
-                        q_lens=[1] * 6, new_lens=[1, 1, 0, 1, 1, 1], num_heads=32, num_kv_heads=8, head_dim=128,
-                        num_blocks=256)
-    out = _check_merged(case, P)
-    assert torch.all(out[2] == 0)
-
-
-def test_splitkv_merged_flags_a_dirty_counter():
-    """A counter that is not zero at entry (e.g. left by an aborted call) is reported as
-    PA_DEV_OUT_OF_RANGE; the other (sequence, kv head) pairs are merged as usual."""
-    case = W.random_case(4400, batch=3, num_heads=32, num_kv_heads=8, head_dim=128, min_len=100, max_len=400)
-    g = GpuCase(case)
-    B, Hq, D = case.q.shape
-    P = 4
-    ws_o = torch.empty((B, Hq, P, D), dtype=torch.float32, device="cuda")
-    ws_lse = torch.empty((B, Hq, P), dtype=torch.float32, device="cuda")
-    arrivals = torch.zeros(B * case.num_kv_heads, dtype=torch.int32, device="cuda")
-    arrivals[5] = 7  # sequence 0, kv head 5
-    out = torch.zeros_like(g.q)
-    pa.pa_decode_splitkv_merged(g.pool, g.q, g.bt, g.sl, case.scale, P, ws_o, ws_lse, arrivals, out)
-    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
-    ref = oracle_decode(case)
-    compare(out[1:], ref[1:], "merged split beside a dirty counter")
-    compare(out[0, :20], ref[0, :20], "merged split, clean kv heads of the same sequence")
 
 
 def test_splitkv_one_partition_equals_decode():
@@ -287,6 +222,28 @@ def test_prefill_ragged_sweep(hq, hkv, d):
         g = GpuCase(case)
         compare(g.prefill(), oracle_prefill(case), f"prefill {hq}/{hkv}/{d} shared {shared}")
     check_status_clean("prefill sweep")
+
+
+def test_prefill_late_dominant_keys_rebase():
+    """Keys far into the cached prefix whose scores exceed everything before them by far more
+    than the lazy re-basing threshold (2^8): rows re-base in stages wholly below the diagonal,
+    which rescales O and the stage's stored P.  Planted by overwriting, in the pool and in the
+    unpaged copy alike, the K rows of tokens 700 and 1500 of every sequence with 4x a query of
+    the chunk (its own score is then about 4|q|^2 scale = 45, against about 1 elsewhere)."""
+    case = W.random_case(5710, batch=3, num_heads=32, num_kv_heads=8, head_dim=128, min_len=1700, max_len=1900,
+                         q_len=256, prefill=True)
+    g_ = case.group
+    for s_, tok in ((0, 700), (1, 1500), (2, 700), (2, 1500)):
+        L = int(case.seq_lens[s_])
+        blk, off = int(case.block_tables[s_, tok // 16]), tok % 16
+        q0 = int(case.cu_q_lens[s_]) + 5
+        for kvh in range(case.num_kv_heads):
+            row = (case.q[q0, kvh * g_].float() * 4).to(torch.bfloat16)
+            case.k_cache[blk, kvh, off] = row
+            case.k_seq[s_][tok, kvh] = row
+    g = GpuCase(case)
+    compare(g.prefill(), oracle_prefill(case), "prefill, late dominant keys (re-base below the diagonal)")
+    check_status_clean("late dominant keys")
 
 
 def test_prefill_one_row_chunk_equals_decode():
