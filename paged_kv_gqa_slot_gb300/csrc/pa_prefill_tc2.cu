@@ -1,5 +1,5 @@
 // pa_prefill_tc2.cu -- chunked prefill over a cached paged prefix on the 5th-generation
-// tensor cores, 128 keys per stage with P kept in tensor memory.
+// tensor cores, with double-buffered scores and P kept in tensor memory.
 //
 // Method: "Qwen3-4B / 8B / 32B", sections "Warm Prefix-Cache TTFT" (a warm prefix hit:
 // only the new chunk is computed, over the cached prefix) and "Architecture Notes" (GQA
@@ -9,31 +9,30 @@
 // Rows of a query tile are (query, head-of-the-group) pairs: row r = query r / g, head r % g,
 // so one K/V tile serves all g heads; a tile holds 128 rows (128 / g queries).  One CTA per
 // SM holds TWO query tiles of the same (sequence, kv head), the i-th longest with the i-th
-// shortest, so every CTA has about the same causal work.  Per stage of 128 keys (eight
+// shortest, so every CTA has about the same causal work.  Per stage of 64 keys (four
 // 16-token pool blocks, loaded by TMA with 128-byte swizzling), for each tile t:
-//   S_t[128 x 128] = Q_t K^T    tcgen05.mma, M=128 N=128, Q_t (A) and K (B) from smem
+//   S_t[128 x 64] = Q_t K^T     tcgen05.mma, M=128 N=64, Q_t (A) and K (B) from smem
 //   softmax          one thread per row reads its S row from TMEM, masks causally (only in
 //                    stages that cross the diagonal), keeps an online max / sum in base 2 and
-//                    writes P (bf16) back into the first 64 columns of S_t in TMEM
+//                    writes P (bf16, two keys per column) over the first 32 columns of S_t
 //   O_t += P_t V     tcgen05.mma, M=128 N=128, P_t (A) from TMEM, V (B) from smem
-// Tensor memory: tile t owns columns [256t, 256t+256): S_t (and P_t over its first half)
-// [0, 128) and O_t [128, 256).  The tensor core runs the MMAs of one CTA in issue order, so
-// the half of S_t(j+1) that P_t(j) shares, keys 0-63, is written only after P_t V(j) has read
-// P_t(j); keys 64-127 are computed as soon as the softmax has read those columns of S_t(j).
-// Per stage j the MMA warp issues, for each tile, S_t(j+1) keys 64-127, then P_t V(j) and S_t(j+1)
-// keys 0-63, so one tile's softmax runs while the other tile's MMAs do.  The running max is
-// re-based lazily: O is rescaled in TMEM only when a row's max grows by more than 2^8, which
-// keeps every P <= 256 and makes rescales rare.
+// Tensor memory: tile t owns columns [256t, 256t+256): two 64-column score buffers, stage j
+// in buffer j % 2, and O_t [128, 256).  So S_t(j+1) is computed while the softmax works on
+// stage j, and P_t V(j) only gates S_t(j+2), which reuses the buffer P_t(j) sits in: the
+// tensor core runs the MMAs of one CTA in issue order, and the MMA warp issues, per stage j
+// and tile t, P_t V(j) then S_t(j+2).  The two tiles' softmax warpgroups run side by side.
+// The running max is re-based lazily: O is rescaled in TMEM only when a row's max grows by
+// more than 2^8, which keeps every P <= 256 and makes rescales rare.
 // Q tiles come in by TMA through a 3-D map of q (d, head, token) whose box is one tile (a tile
 // cut short by the end of its chunk row by row instead); each row of O is stored by its thread.
 // Warp roles: 0-3 softmax of tile 0, 4-7 softmax of tile 1 (TMEM lanes 32(w%4)..+31),
-// 8 MMA issue + TMEM owner, 9 TMA loads of K, 10 TMA loads of V.  Every CTA loads its own
-// K/V; the CTAs of one (sequence, kv head) -- and, with a shared prefix, of every sequence
-// that shares it -- read the same pool blocks, the copies after the first from L2.
+// 8 MMA issue + TMEM owner, 9 TMA loads of K, 10 TMA loads of V, 11 idle (it completes the
+// control warpgroup, which hands registers to the softmax warpgroups).  Every CTA loads its
+// own K/V; the CTAs of one (sequence, kv head) -- and, with a shared prefix, of every
+// sequence that shares it -- read the same pool blocks, the copies after the first from L2.
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
-#include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -44,34 +43,42 @@ namespace {
 constexpr int kD = 128;
 constexpr int kRows = 128;                      // MMA M: rows of one query tile
 constexpr int kTiles = 2;                       // query tiles per CTA
-constexpr int kKeys = 128;                      // keys per stage (MMA N of S, K of P V)
-constexpr int kKStages = 3;                     // K ring slots: S(j+1)'s upper half starts early
-constexpr int kVStages = 2;                     // V ring slots
+constexpr int kKeys = 64;                       // keys per stage (MMA N of S, K of P V)
+constexpr int kKStages = 4, kVStages = 4;       // K and V ring slots
 constexpr int kSoftmaxThreads = kTiles * 128;
 constexpr int kMmaWarp = kSoftmaxThreads / 32, kKLoadWarp = kMmaWarp + 1, kVLoadWarp = kMmaWarp + 2;
-constexpr int kThreads = kSoftmaxThreads + 96;
+constexpr int kThreads = kSoftmaxThreads + 128;   // + a control warpgroup: MMA, K, V, idle
+// Registers: launched at kLaunchRegs a thread (65536 / 384 threads), the control warpgroup
+// gives some back and the softmax warpgroups take them (setmaxnreg); the shares add up to
+// exactly the launch's total, and the launcher checks the compiled count.
+constexpr int kLaunchRegs = 168, kSoftmaxRegs = 208, kControlRegs = 88;
+static_assert(kSoftmaxThreads * kSoftmaxRegs + 128 * kControlRegs == kThreads * kLaunchRegs, "register split");
 constexpr int kTmemCols = 512;
 constexpr uint32_t kTmemTile = 256;             // columns owned by one tile
-constexpr uint32_t kTmemS = 0, kTmemO = 128;
-constexpr int kHalfBytes = 128 * 128;           // [128 rows][64 columns] bf16 = 16 KB
-constexpr int kTileBytes = 2 * kHalfBytes;      // a Q tile, or one K or V stage: two column halves
+constexpr uint32_t kTmemS = 0, kTmemO = 128;    // score buffers at 0 and 64, O at 128
+constexpr int kQHalf = kRows * 128;             // [128 rows][64 columns] bf16 = 16 KB
+constexpr int kQTile = 2 * kQHalf;              // a Q tile: two column halves
+constexpr int kKVHalf = kKeys * 128;            // [64 keys][64 columns] bf16 = 8 KB
+constexpr int kKVStage = 2 * kKVHalf;           // one K or V stage: two column halves
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTiles * kTileBytes;
-constexpr int kOffV = kOffK + kKStages * kTileBytes;
-constexpr int kBarOff = kOffV + kVStages * kTileBytes;
+constexpr int kOffK = kOffQ + kTiles * kQTile;
+constexpr int kOffV = kOffK + kKStages * kKVStage;
+constexpr int kBarOff = kOffV + kVStages * kKVStage;
 constexpr int kSmemBytes = kBarOff + 256 + 1024;
-constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.f;        // log2 units
+constexpr float kLog2e = 1.44269504088896340736f;
 
 struct Bars {
     uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
-    uint64_t q_full[kTiles], s_full[kTiles], s_hi_free[kTiles], p_full[kTiles], o_done[kTiles];
+    // per tile: scores and P of stage j use buffer j % 2 (a softmax may finish two stages before
+    // the MMA warp waits for the first, so one barrier per buffer keeps their phases apart);
+    // o_done completes after every P V, o_final after the tile's last one
+    uint64_t q_full[kTiles], s_full[kTiles][2], p_full[kTiles][2], o_done[kTiles], o_final[kTiles];
     uint64_t drain;
     uint32_t tmem_base;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-static_assert(kRows == kKeys, "one 16 KB half layout for Q tiles and K/V stages");
 
 struct Tc2Args {
     const __nv_bfloat16* q;
@@ -113,6 +120,20 @@ __device__ __forceinline__ bool named_sync_all(int id, int count, bool pred) {
     return r != 0;
 }
 
+// O (the row's 128 fp32 columns of tensor memory at `taddr`) *= f, in 8-column pieces.
+__device__ __forceinline__ void scale_o(uint32_t taddr, float f) {
+#pragma unroll 1
+    for (int c = 0; c < kD; c += 8) {
+        uint32_t o[8];
+        tmem_ld8(taddr + c, o);
+        tmem_st8_nowait(taddr + c, __float_as_uint(__uint_as_float(o[0]) * f), __float_as_uint(__uint_as_float(o[1]) * f),
+                        __float_as_uint(__uint_as_float(o[2]) * f), __float_as_uint(__uint_as_float(o[3]) * f),
+                        __float_as_uint(__uint_as_float(o[4]) * f), __float_as_uint(__uint_as_float(o[5]) * f),
+                        __float_as_uint(__uint_as_float(o[6]) * f), __float_as_uint(__uint_as_float(o[7]) * f));
+    }
+    tmem_wait_st();
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                   const __grid_constant__ CUtensorMap tm_v,
                                                                   const __grid_constant__ CUtensorMap tm_q,
@@ -152,10 +173,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(&bars->q_full[t], 1);
-            mbar_init(&bars->s_full[t], 1);
-            mbar_init(&bars->s_hi_free[t], 128);
-            mbar_init(&bars->p_full[t], 128);
+            mbar_init(&bars->s_full[t][0], 1);
+            mbar_init(&bars->s_full[t][1], 1);
+            mbar_init(&bars->p_full[t][0], 128);
+            mbar_init(&bars->p_full[t][1], 128);
             mbar_init(&bars->o_done[t], 1);
+            mbar_init(&bars->o_final[t], 1);
         }
         mbar_init(&bars->drain, 1);
         fence_mbar_init();
@@ -169,142 +192,140 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    if (warp == kKLoadWarp || warp == kVLoadWarp) {
-        // ------------------------------------------------------------ TMA producers (K, V)
-        // The 16 boxes of a stage (8 blocks x 2 column halves, 2 KB each) go out from lanes
-        // 0-15, one each; a block past the keys the pair needs reads past the pool (zeros).
-        const bool is_k = warp == kKLoadWarp;
-        const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-        uint64_t* full = is_k ? bars->k_full : bars->v_full;
-        uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
-        uint8_t* ring = smem + (is_k ? kOffK : kOffV);
-        const int nslots = is_k ? kKStages : kVStages;
-        if (lane == 0) prefetch_tensormap(map);
-        const uint64_t pol = l2_evict_last_policy();  // prefix blocks are shared across sequences
-        const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks;
-        const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;
-        int c0 = 0;
-        int cur = lane < nblk ? __ldg(bt + lane) : 0;
-        int nxt = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
-        const int box_t = lane >> 1, box_h = lane & 1;
-        bool ok = true;
-        int issued = 0;
-        for (int j = 0; j < nstage && ok; ++j) {
-            if (8 * j >= c0 + 32) {
-                c0 += 32;
-                cur = nxt;
-                nxt = c0 + 32 + lane < nblk ? __ldg(bt + c0 + 32 + lane) : 0;
+    if (warp >= kMmaWarp) {
+        // control warpgroup: every warp gives registers back at this one point, then takes its role
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+        if (warp == kKLoadWarp || warp == kVLoadWarp) {
+            // -------------------------------------------------------- TMA producers (K, V)
+            // The 8 boxes of a stage (4 blocks x 2 column halves, 2 KB each) go out from lanes
+            // 0-7, one each; a block past the keys the pair needs reads past the pool (zeros).
+            const bool is_k = warp == kKLoadWarp;
+            const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+            uint64_t* full = is_k ? bars->k_full : bars->v_full;
+            uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+            uint8_t* ring = smem + (is_k ? kOffK : kOffV);
+            const int nslots = is_k ? kKStages : kVStages;
+            if (lane == 0) prefetch_tensormap(map);
+            const uint64_t pol = l2_evict_last_policy();  // prefix blocks are shared across sequences
+            const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks;
+            const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;
+            int c0 = 0;
+            int cur = lane < nblk ? __ldg(bt + lane) : 0;
+            int nxt = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
+            const int box_t = lane >> 1, box_h = lane & 1;
+            bool ok = true;
+            int issued = 0;
+            for (int j = 0; j < nstage && ok; ++j) {
+                if (4 * j >= c0 + 32) {
+                    c0 += 32;
+                    cur = nxt;
+                    nxt = c0 + 32 + lane < nblk ? __ldg(bt + c0 + 32 + lane) : 0;
+                }
+                if (is_k && c0 + lane < nblk && (cur < 0 || cur >= a.num_blocks)) atomicOr(a.status, kDevOutOfRange);
+                if (cur < 0 || cur >= a.num_blocks) cur = 0;
+                const int lb = 4 * j + box_t;
+                const int id = __shfl_sync(0xffffffffu, cur, (lb - c0) & 31);
+                const int row = lb < nblk ? (id * a.num_kv_heads + kvh) * kBlockSize : oob_row;
+                const int s = j % nslots;
+                if (lane == 0) {
+                    if (j >= nslots) ok = mbar_wait(&empty[s], ((j / nslots) & 1) ^ 1);
+                    if (ok) mbar_arrive_expect_tx(&full[s], kKVStage);
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+                if (ok) {
+                    if (lane < 8)
+                        tma_load_2d(ring + s * kKVStage + box_h * kKVHalf + box_t * 2048, map, box_h * 64, row,
+                                    &full[s], pol);
+                    ++issued;
+                }
             }
-            if (is_k && c0 + lane < nblk && (cur < 0 || cur >= a.num_blocks)) atomicOr(a.status, kDevOutOfRange);
-            if (cur < 0 || cur >= a.num_blocks) cur = 0;
-            const int lb = 8 * j + box_t;
-            const int id = __shfl_sync(0xffffffffu, cur, (lb - c0) & 31);
-            const int row = lb < nblk ? (id * a.num_kv_heads + kvh) * kBlockSize : oob_row;
-            const int s = j % nslots;
             if (lane == 0) {
-                if (j >= nslots) ok = mbar_wait(&empty[s], ((j / nslots) & 1) ^ 1);
-                if (ok) mbar_arrive_expect_tx(&full[s], kTileBytes);
+                // before the CTA may leave: every box issued here has landed
+                for (int j = max(0, issued - nslots); j < issued; ++j)
+                    if (!mbar_wait(&full[j % nslots], (j / nslots) & 1)) ok = false;
+                if (!ok) atomicOr(a.status, kDevTimeout);
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
-            if (ok) {
-                if (lane < 16)
-                    tma_load_2d(ring + s * kTileBytes + box_h * kHalfBytes + box_t * 2048, map, box_h * 64, row,
-                                &full[s], pol);
-                ++issued;
-            }
-        }
-        if (lane == 0) {
-            // before the CTA may leave: every box issued here has landed
-            for (int j = max(0, issued - nslots); j < issued; ++j)
-                if (!mbar_wait(&full[j % nslots], (j / nslots) & 1)) ok = false;
-            if (!ok) atomicOr(a.status, kDevTimeout);
-        }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------------ MMA issue (whole warp)
-        // The warp runs the loop together and one elected lane issues, so every operand is
-        // warp-uniform; waits give one verdict for the warp.  Operand descriptors are built
-        // once; a tile, a stage or a k-step only moves the start address, which adds
-        // (offset >> 4) to the low field (no carry: every shared address is below 2^18).
-        constexpr uint32_t idesc_s = tc_idesc_bf16(kRows, kKeys, false);
-        constexpr uint32_t idesc_h = tc_idesc_bf16(kRows, kKeys / 2, false);
-        constexpr uint32_t idesc_o = tc_idesc_bf16(kRows, kD, true);
-        const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem + kOffQ), 0, 1024);
-        const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + kOffK), 0, 1024);
-        const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + kOffV), kHalfBytes, 1024);
-        // S_t = Q_t K(j)^T over keys [64 h0, 64 (h0 + nh)): N = 64 nh, into S_t's columns from 64 h0
-        auto issue_qk = [&](int t, int j, int h0, int nh) {
-            const uint64_t qd = qdesc0 + (uint64_t)((t * kTileBytes) >> 4);
-            const uint64_t kd = kdesc0 + (uint64_t)(((j % kKStages) * kTileBytes + h0 * (kHalfBytes / 2)) >> 4);
-            const uint32_t tm_s = tmem + t * kTmemTile + kTmemS + 64 * h0;
+        } else if (warp == kMmaWarp) {
+            // -------------------------------------------------------- MMA issue (whole warp)
+            // The warp runs the loop together and one elected lane issues, so every operand is
+            // warp-uniform; waits give one verdict for the warp.  Operand descriptors are built
+            // once; a tile, a stage or a k-step only moves the start address, which adds
+            // (offset >> 4) to the low field (no carry: every shared address is below 2^18).
+            constexpr uint32_t idesc_s = tc_idesc_bf16(kRows, kKeys, false);
+            constexpr uint32_t idesc_o = tc_idesc_bf16(kRows, kD, true);
+            const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem + kOffQ), 0, 1024);
+            const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + kOffK), 0, 1024);
+            const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + kOffV), kKVHalf, 1024);
+            auto issue_qk = [&](int t, int j) {  // S_t(j) = Q_t K(j)^T into score buffer j % 2
+                const uint64_t qd = qdesc0 + (uint64_t)((t * kQTile) >> 4);
+                const uint64_t kd = kdesc0 + (uint64_t)(((j % kKStages) * kKVStage) >> 4);
+                const uint32_t tm_s = tmem + t * kTmemTile + kTmemS + 64 * (j & 1);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint64_t off = (uint64_t)(((kk >> 2) * kHalfBytes + (kk & 3) * 32) >> 4);
-                tc_mma_ew(tm_s, qd + off, kd + off, nh == 2 ? idesc_s : idesc_h, kk > 0 ? 1u : 0u);
-            }
-        };
-        auto issue_pv = [&](int t, int j) {  // O_t += P_t V(j), P_t from tensor memory
-            const uint64_t vd = vdesc0 + (uint64_t)(((j % kVStages) * kTileBytes) >> 4);
-            const uint32_t tm_p = tmem + t * kTmemTile + kTmemS, tm_o = tmem + t * kTmemTile + kTmemO;
+                for (int kk = 0; kk < kD / 16; ++kk)
+                    tc_mma_ew(tm_s, qd + (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
+                              kd + (uint64_t)(((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idesc_s, kk > 0 ? 1u : 0u);
+                tc_commit_ew(&bars->s_full[t][j & 1]);
+            };
+            auto issue_pv = [&](int t, int j) {  // O_t += P_t(j) V(j), P_t(j) in score buffer j % 2
+                const uint64_t vd = vdesc0 + (uint64_t)(((j % kVStages) * kKVStage) >> 4);
+                const uint32_t tm_p = tmem + t * kTmemTile + kTmemS + 64 * (j & 1);
+                const uint32_t tm_o = tmem + t * kTmemTile + kTmemO;
 #pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk)
-                tc_mma_ts_ew(tm_o, tm_p + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
-                             (j > 0 || kk > 0) ? 1u : 0u);
-            tc_commit_ew(&bars->o_done[t]);
-        };
-        bool ok = true;
-#pragma unroll
-        for (int t = 0; t < kTiles; ++t)
-            if (ok && nst[t] > 0) ok = mbar_wait_warp(&bars->q_full[t], 0);
-        if (ok) ok = mbar_wait_warp(&bars->k_full[0], 0);
-        if (ok) {
-            tc_fence_after();
+                for (int kk = 0; kk < kKeys / 16; ++kk)
+                    tc_mma_ts_ew(tm_o, tm_p + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                                 (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit_ew(&bars->o_done[t]);
+                if (j + 1 == nst[t]) tc_commit_ew(&bars->o_final[t]);
+            };
+            bool ok = true;
 #pragma unroll
             for (int t = 0; t < kTiles; ++t)
-                if (nst[t] > 0) {
-                    issue_qk(t, 0, 0, 2);
-                    tc_commit_ew(&bars->s_full[t]);
-                }
-            tc_commit_ew(&bars->k_empty[0]);  // S(0) is K(0)'s only reader
-        }
-        for (int j = 0; j < nstage && ok; ++j) {
-            bool v_ready = false, k_next = false;
+                if (ok && nst[t] > 0) ok = mbar_wait_warp(&bars->q_full[t], 0);
+            // stages 0 and 1 of both tiles into the two score buffers
+            for (int j = 0; j < 2 && j < nstage && ok; ++j) {
+                ok = mbar_wait_warp(&bars->k_full[j], 0);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-            for (int t = 0; t < kTiles; ++t) {
-                if (!ok || j >= nst[t]) continue;
-                const bool more = j + 1 < nst[t];
-                if (more) {
-                    // keys 64-127 of S_t(j+1) once the softmax has read those columns of S_t(j)
-                    ok = mbar_wait_warp(&bars->s_hi_free[t], j & 1);
-                    if (ok && !k_next) {
-                        ok = mbar_wait_warp(&bars->k_full[(j + 1) % kKStages], ((j + 1) / kKStages) & 1);
-                        k_next = true;
+                for (int t = 0; t < kTiles; ++t)
+                    if (j < nst[t]) issue_qk(t, j);
+                tc_commit_ew(&bars->k_empty[j]);  // K(j) is read by S(j) of both tiles only
+            }
+            for (int j = 0; j < nstage && ok; ++j) {
+                bool v_ready = false, k_ready = false;
+#pragma unroll
+                for (int t = 0; t < kTiles; ++t) {
+                    if (!ok || j >= nst[t]) continue;
+                    ok = mbar_wait_warp(&bars->p_full[t][j & 1], (j >> 1) & 1);
+                    if (ok && !v_ready) {
+                        ok = mbar_wait_warp(&bars->v_full[j % kVStages], (j / kVStages) & 1);
+                        v_ready = true;
                     }
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk(t, j + 1, 1, 1);
-                }
-                ok = mbar_wait_warp(&bars->p_full[t], j & 1);
-                if (ok && !v_ready) {
-                    ok = mbar_wait_warp(&bars->v_full[j % kVStages], (j / kVStages) & 1);
-                    v_ready = true;
+                    issue_pv(t, j);
+                    if (j + 2 < nst[t]) {
+                        // S_t(j+2) reuses the buffer P_t(j) sits in: after P_t V(j) in issue order
+                        if (!k_ready) {
+                            ok = mbar_wait_warp(&bars->k_full[(j + 2) % kKStages], ((j + 2) / kKStages) & 1);
+                            k_ready = true;
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        issue_qk(t, j + 2);
+                    }
                 }
                 if (!ok) break;
-                tc_fence_after();
-                issue_pv(t, j);
-                if (more) {
-                    issue_qk(t, j + 1, 0, 1);  // keys 0-63, over P_t(j): after P_t V(j) in issue order
-                    tc_commit_ew(&bars->s_full[t]);
-                }
+                tc_commit_ew(&bars->v_empty[j % kVStages]);
+                if (k_ready) tc_commit_ew(&bars->k_empty[(j + 2) % kKStages]);
             }
-            if (!ok) break;
-            tc_commit_ew(&bars->v_empty[j % kVStages]);
-            if (k_next) tc_commit_ew(&bars->k_empty[(j + 1) % kKStages]);  // K(j+1)'s last reader is issued
+            // every MMA issued above has finished before the tensor memory is released
+            tc_commit_ew(&bars->drain);
+            if (!mbar_wait_warp(&bars->drain, 0)) ok = false;
+            if (!ok && lane == 0) atomicOr(a.status, kDevTimeout);
         }
-        // every MMA issued above has finished before the tensor memory is released
-        tc_commit_ew(&bars->drain);
-        if (!mbar_wait_warp(&bars->drain, 0)) ok = false;
-        if (!ok && lane == 0) atomicOr(a.status, kDevTimeout);
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         // ------------------------------------------------------------ softmax: one row per thread
         const int t = warp >> 2;                    // query tile of this warpgroup
         const int r = threadIdx.x & (kRows - 1);    // TMEM lane r, MMA row r
@@ -317,15 +338,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         const int pos = valid ? L - C + tok0 + qi : -1;  // causal limit of the row (inclusive)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tm_row = tmem + lane_base + t * kTmemTile;
-        uint8_t* qs = smem + kOffQ + t * kTileBytes;
+        uint8_t* qs = smem + kOffQ + t * kQTile;
         const int bar_id = 1 + t;                   // named barrier of this warpgroup
         if (nt > 0) {
             if (whole) {
                 if (r == 0) {
                     prefetch_tensormap(&tm_q);
-                    mbar_arrive_expect_tx(&bars->q_full[t], kTileBytes);
+                    mbar_arrive_expect_tx(&bars->q_full[t], kQTile);
                     tma_load_3d(qs, &tm_q, 0, kvh * g, q0 + tok0, &bars->q_full[t]);
-                    tma_load_3d(qs + kHalfBytes, &tm_q, 64, kvh * g, q0 + tok0, &bars->q_full[t]);
+                    tma_load_3d(qs + kQHalf, &tm_q, 64, kvh * g, q0 + tok0, &bars->q_full[t]);
                 }
             } else {
                 // row by row into the same 128-byte swizzled layout (zeros past the chunk)
@@ -335,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                 for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(qs + hh * kHalfBytes + swz128(r, c)) =
+                        *reinterpret_cast<uint4*>(qs + hh * kQHalf + swz128(r, c)) =
                             valid ? __ldg(src + hh * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
                 fence_proxy_async_smem();
                 named_sync(bar_id, 128);
@@ -350,222 +371,107 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         // tcgen05.ld / tcgen05.st are warp-collective: every decision that leads to one (a wait
         // that gave up, a rescale of O) is taken by the whole warp.
         for (int j = 0; j < nt; ++j) {
-            if (__any_sync(0xffffffffu, !mbar_wait(&bars->s_full[t], j & 1))) {
+            const uint32_t sbuf = tm_row + kTmemS + 64 * (j & 1);
+            if (__any_sync(0xffffffffu, !mbar_wait(&bars->s_full[t][j & 1], (j >> 1) & 1))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const int k0 = j * kKeys;
             const int lim = pos - k0;  // keys c <= lim of this stage are visible to the row
-            // Stages wholly below the diagonal (every row of the warp sees all 128 keys) after
-            // the first take the streaming path; the first stage and the diagonal ones the
-            // careful path.  Both write P (rounded to bf16, two keys per tensor-memory column,
-            // the layout P V reads) into the first 64 columns of S_t, and add the rounded
-            // values to the row sum, so the weights P V uses sum to l.
-            const bool stream = j > 0 && __all_sync(0xffffffffu, lim >= kKeys - 1);
-            // p = 2^(s scale log2(e) - m) for 4 keys: one packed multiply-add per two keys, the
-            // special-function unit, bf16 packing; the packed words' values go to the sum
-            auto p4 = [&](float v0, float v1, float v2, float v3, float nbase, bool m0, bool m1, bool m2, bool m3,
-                          uint32_t& w0, uint32_t& w1, float (&ls)[4]) {
-                float x0, x1, x2, x3;
-                fma_x2(x0, x1, v0, v1, sl, sl, nbase, nbase);
-                fma_x2(x2, x3, v2, v3, sl, sl, nbase, nbase);
-                float q0 = fast_exp2(x0), q1 = fast_exp2(x1), q2 = fast_exp2(x2), q3 = fast_exp2(x3);
-                q0 = m0 ? 0.f : q0;
-                q1 = m1 ? 0.f : q1;
-                q2 = m2 ? 0.f : q2;
-                q3 = m3 ? 0.f : q3;
-                w0 = pack_bf16x2(q0, q1);
-                w1 = pack_bf16x2(q2, q3);
-                add_x2(ls[0], ls[1], bf16_lo(w0), bf16_hi(w0));
-                add_x2(ls[2], ls[3], bf16_lo(w1), bf16_hi(w1));
+            // Stages wholly below the diagonal (every row of the warp sees all 64 keys) need no
+            // mask; only they are common.  The choice of path below rests on the vote alone: a
+            // row whose own limit happens to be 64 must not take the unmasked path by itself.
+            const bool unmasked = __all_sync(0xffffffffu, lim >= kKeys - 1);
+            const int mlim = unmasked ? kKeys : lim;
+            // p = 2^(s scale log2(e) - m), rounded to bf16, two keys to a 32-bit word (the layout
+            // P V reads from tensor memory): one packed multiply-add per two keys, the
+            // special-function unit, bf16 packing
+            uint32_t pw[kKeys / 2];
+            auto exps = [&](int c, const uint32_t (&sr)[32], float nbase) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const int kb = c * 32 + e;
+                    float x0, x1, x2, x3;
+                    fma_x2(x0, x1, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]), sl, sl, nbase, nbase);
+                    fma_x2(x2, x3, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]), sl, sl, nbase, nbase);
+                    float e0 = fast_exp2(x0), e1 = fast_exp2(x1), e2 = fast_exp2(x2), e3 = fast_exp2(x3);
+                    e0 = kb > mlim ? 0.f : e0;
+                    e1 = kb + 1 > mlim ? 0.f : e1;
+                    e2 = kb + 2 > mlim ? 0.f : e2;
+                    e3 = kb + 3 > mlim ? 0.f : e3;
+                    pw[kb / 2] = pack_bf16x2(e0, e1);
+                    pw[kb / 2 + 1] = pack_bf16x2(e2, e3);
+                }
             };
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            if (stream) {
-                // S in 32-key pieces, the next piece's load in flight; the row maximum of the
-                // (sign-adjusted) scores is tracked beside the exponentials, which use the
-                // running base.  P is held in registers until the stage's maximum is known: a
-                // row whose maximum outgrows the base recomputes it from S with the new base
-                // (computing it against the old one and rescaling would round it twice).
-                float nbase = -m_used;
-                float m8[8];
+            // row maximum of the sign-adjusted scores over keys <= mlim (|scale| keeps the order
+            // of s, or reverses it for a negative scale, where it is taken over -s), 4 chains
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            auto maxs = [&](int c, const uint32_t (&sr)[32]) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-                uint32_t pw[kKeys / 2];
-                auto piece = [&](int c, const uint32_t (&sr)[32], bool with_max) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float v0 = __uint_as_float(sr[e]), v1 = __uint_as_float(sr[e + 1]);
-                        const float v2 = __uint_as_float(sr[e + 2]), v3 = __uint_as_float(sr[e + 3]);
-                        if (with_max) {
-                            const int ch = (e >> 2) & 3;
-                            m8[2 * ch] = fmax3(m8[2 * ch], neg ? -v0 : v0, neg ? -v1 : v1);
-                            m8[2 * ch + 1] = fmax3(m8[2 * ch + 1], neg ? -v2 : v2, neg ? -v3 : v3);
-                        }
-                        float x0, x1, x2, x3;
-                        fma_x2(x0, x1, v0, v1, sl, sl, nbase, nbase);
-                        fma_x2(x2, x3, v2, v3, sl, sl, nbase, nbase);
-                        pw[(c * 32 + e) / 2] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
-                        pw[(c * 32 + e) / 2 + 1] = pack_bf16x2(fast_exp2(x2), fast_exp2(x3));
-                    }
-                };
-                auto pass = [&](bool with_max) {
-                    uint32_t sa[32], sb[32];
-                    tmem_ld32_async(tm_row + kTmemS, sa);
-                    tmem_wait_ld(sa);
-                    tmem_ld32_async(tm_row + kTmemS + 32, sb);
-                    piece(0, sa, with_max);
-                    tmem_wait_ld(sb);
-                    tmem_ld32_async(tm_row + kTmemS + 64, sa);
-                    piece(1, sb, with_max);
-                    tmem_wait_ld(sa);
-                    tmem_ld32_async(tm_row + kTmemS + 96, sb);
-                    piece(2, sa, with_max);
-                    tmem_wait_ld(sb);
-                    piece(3, sb, with_max);
-                };
-                pass(true);
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                const float m_new = fmaxf(m_used, mx * sl_abs);
-                const bool rebase = m_new > m_used + kRescaleThreshold;
-                if (__any_sync(0xffffffffu, rebase)) {
-                    // Rare: some row's maximum outgrew its base.  O_t is still (P_t V(j-1) was
-                    // issued before S_t(j), whose commit covers it), so rescale it; then P again,
-                    // every row against its own base (unchanged rows get the same bits).
-                    const float alpha = rebase ? fast_exp2(m_used - m_new) : 1.f;
-#pragma unroll 1
-                    for (int c = 0; c < kD; c += 8) {
-                        uint32_t o[8];
-                        tmem_ld8(tm_row + kTmemO + c, o);
-                        tmem_st8_nowait(tm_row + kTmemO + c, __float_as_uint(__uint_as_float(o[0]) * alpha),
-                                        __float_as_uint(__uint_as_float(o[1]) * alpha),
-                                        __float_as_uint(__uint_as_float(o[2]) * alpha),
-                                        __float_as_uint(__uint_as_float(o[3]) * alpha),
-                                        __float_as_uint(__uint_as_float(o[4]) * alpha),
-                                        __float_as_uint(__uint_as_float(o[5]) * alpha),
-                                        __float_as_uint(__uint_as_float(o[6]) * alpha),
-                                        __float_as_uint(__uint_as_float(o[7]) * alpha));
-                    }
-                    tmem_wait_st();
-                    if (rebase) {
-                        l *= alpha;
-                        m_used = m_new;
-                    }
-                    nbase = -m_used;
-                    pass(false);
+                for (int e = 0; e < 32; e += 2) {
+                    const int kb = c * 32 + e;
+                    float a0 = __uint_as_float(sr[e]), a1 = __uint_as_float(sr[e + 1]);
+                    a0 = kb > mlim ? -INFINITY : (neg ? -a0 : a0);
+                    a1 = kb + 1 > mlim ? -INFINITY : (neg ? -a1 : a1);
+                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], a0, a1);
                 }
-                tc_fence_before();
-                mbar_arrive(&bars->s_hi_free[t]);  // S_t's columns 64-127 are read
-                // the row sum adds the rounded values P V uses; P goes over S_t's first half
-#pragma unroll
-                for (int w = 0; w < kKeys / 2; w += 2) {
-                    add_x2(ls[0], ls[1], bf16_lo(pw[w]), bf16_hi(pw[w]));
-                    add_x2(ls[2], ls[3], bf16_lo(pw[w + 1]), bf16_hi(pw[w + 1]));
-                }
-#pragma unroll
-                for (int i = 0; i < kKeys / 16; ++i)
-                    tmem_st8_nowait(tm_row + kTmemS + 8 * i, pw[8 * i], pw[8 * i + 1], pw[8 * i + 2], pw[8 * i + 3],
-                                    pw[8 * i + 4], pw[8 * i + 5], pw[8 * i + 6], pw[8 * i + 7]);
-                tmem_wait_st();
-            } else {
-                // Two passes over S in 32-key pieces: the maximum over the visible keys, then
-                // the exponentials against the (re-based if need be) base.
-                float m8[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) m8[e] = -INFINITY;
-                // per-key masking only where some row of the warp sees part of the stage
-                const bool masked = !__all_sync(0xffffffffu, lim >= kKeys - 1);
-                const int mlim = masked ? lim : kKeys;
-                auto max_piece = [&](int c, const uint32_t (&sr)[32]) {
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const int kb = c * 32 + e;
-                        float a0 = __uint_as_float(sr[e]), a1 = __uint_as_float(sr[e + 1]);
-                        float a2 = __uint_as_float(sr[e + 2]), a3 = __uint_as_float(sr[e + 3]);
-                        a0 = kb > mlim ? -INFINITY : (neg ? -a0 : a0);
-                        a1 = kb + 1 > mlim ? -INFINITY : (neg ? -a1 : a1);
-                        a2 = kb + 2 > mlim ? -INFINITY : (neg ? -a2 : a2);
-                        a3 = kb + 3 > mlim ? -INFINITY : (neg ? -a3 : a3);
-                        const int ch = (e >> 2) & 3;
-                        m8[2 * ch] = fmax3(m8[2 * ch], a0, a1);
-                        m8[2 * ch + 1] = fmax3(m8[2 * ch + 1], a2, a3);
+            };
+            uint32_t s0[32], s1[32];
+            tmem_ld32_async(sbuf, s0);
+            tmem_ld32_async(sbuf + 32, s1);
+            tmem_wait_ld(s0);
+            tmem_wait_ld(s1);
+            // Below the diagonal after the first stage, the exponentials go against the running
+            // base beside the maximum; a row whose maximum outgrows the base does them again
+            // with the new one (computing them against the old one and rescaling would round
+            // them twice).  Elsewhere the maximum comes first.
+            const bool spec = j > 0 && unmasked;  // warp-uniform: the branches below are collective
+            if (spec) {
+                exps(0, s0, -m_used);
+                exps(1, s1, -m_used);
+            }
+            maxs(0, s0);
+            maxs(1, s1);
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            const float mxs = mx == -INFINITY ? -INFINITY : mx * sl_abs;  // log2 units
+            const float m_new = fmaxf(m_used, mxs);
+            const bool rebase = m_new > m_used + kRescaleThreshold;  // always for the first visible key
+            if (__any_sync(0xffffffffu, rebase) || !spec) {
+                if (__any_sync(0xffffffffu, rebase && m_used != -INFINITY)) {
+                    // O_t changes only once P_t V(j-1) -- which may still run, since S_t(j) was
+                    // ready long before -- has finished: its commit is o_done phase j-1 (phases
+                    // up to j-2 are complete, as S_t(j) was issued after P_t V(j-2), and P_t V(j)
+                    // waits for this stage's P, so the parity cannot alias)
+                    if (j > 0 && __any_sync(0xffffffffu, !mbar_wait(&bars->o_done[t], (j - 1) & 1))) {
+                        ok = false;
+                        break;
                     }
-                };
-                {
-                    uint32_t sa[32], sb[32];
-                    tmem_ld32_async(tm_row + kTmemS, sa);
-                    tmem_wait_ld(sa);
-                    tmem_ld32_async(tm_row + kTmemS + 32, sb);
-                    max_piece(0, sa);
-                    tmem_wait_ld(sb);
-                    tmem_ld32_async(tm_row + kTmemS + 64, sa);
-                    max_piece(1, sb);
-                    tmem_wait_ld(sa);
-                    tmem_ld32_async(tm_row + kTmemS + 96, sb);
-                    max_piece(2, sa);
-                    tmem_wait_ld(sb);
-                    max_piece(3, sb);
+                    tc_fence_after();
+                    scale_o(tm_row + kTmemO, rebase && m_used != -INFINITY ? fast_exp2(m_used - m_new) : 1.f);
                 }
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-                const float mxs = mx == -INFINITY ? -INFINITY : mx * sl_abs;  // log2 units
-                const float m_new = fmaxf(m_used, mxs);
-                const bool rescale = m_new > m_used + kRescaleThreshold;  // always for the first visible key
-                const float alpha = rescale && m_used != -INFINITY ? fast_exp2(m_used - m_new) : 0.f;
-                if (__any_sync(0xffffffffu, rescale && m_used != -INFINITY)) {
-                    // O_t is still: see above
-                    const float f = rescale ? alpha : 1.f;
-#pragma unroll 1
-                    for (int c = 0; c < kD; c += 8) {
-                        uint32_t o[8];
-                        tmem_ld8(tm_row + kTmemO + c, o);
-                        tmem_st8_nowait(tm_row + kTmemO + c, __float_as_uint(__uint_as_float(o[0]) * f),
-                                        __float_as_uint(__uint_as_float(o[1]) * f),
-                                        __float_as_uint(__uint_as_float(o[2]) * f),
-                                        __float_as_uint(__uint_as_float(o[3]) * f),
-                                        __float_as_uint(__uint_as_float(o[4]) * f),
-                                        __float_as_uint(__uint_as_float(o[5]) * f),
-                                        __float_as_uint(__uint_as_float(o[6]) * f),
-                                        __float_as_uint(__uint_as_float(o[7]) * f));
-                    }
-                    tmem_wait_st();
-                }
-                if (rescale) {
-                    l *= alpha;  // 0 when nothing was visible before
+                if (rebase) {
+                    l *= m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
                     m_used = m_new;
                 }
                 const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-                auto exp_piece = [&](int c, const uint32_t (&sr)[32]) {
-                    uint32_t w[16];
+                exps(0, s0, nbase);
+                exps(1, s1, nbase);
+            }
+            // The row sum adds the rounded values, so the weights P V uses sum to l; then P goes
+            // over the first 32 columns of the stage's buffer.
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const int kb = c * 32 + e;
-                        p4(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1]), __uint_as_float(sr[e + 2]),
-                           __uint_as_float(sr[e + 3]), nbase, kb > mlim, kb + 1 > mlim, kb + 2 > mlim, kb + 3 > mlim,
-                           w[e / 2], w[e / 2 + 1], ls);
-                    }
-                    tmem_st8_nowait(tm_row + kTmemS + 16 * c, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-                    tmem_st8_nowait(tm_row + kTmemS + 16 * c + 8, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
-                };
-                uint32_t sa[32], sb[32];
-                tmem_ld32_async(tm_row + kTmemS, sa);
-                tmem_wait_ld(sa);
-                tmem_ld32_async(tm_row + kTmemS + 32, sb);
-                exp_piece(0, sa);
-                tmem_wait_ld(sb);
-                tmem_ld32_async(tm_row + kTmemS + 64, sa);
-                exp_piece(1, sb);
-                tmem_wait_ld(sa);
-                tmem_ld32_async(tm_row + kTmemS + 96, sb);
-                exp_piece(2, sa);
-                tmem_wait_ld(sb);
-                tc_fence_before();
-                mbar_arrive(&bars->s_hi_free[t]);  // S_t's columns 64-127 are read
-                exp_piece(3, sb);
-                tmem_wait_st();
+            for (int w = 0; w < kKeys / 2; w += 2) {
+                add_x2(ls[0], ls[1], bf16_lo(pw[w]), bf16_hi(pw[w]));
+                add_x2(ls[2], ls[3], bf16_lo(pw[w + 1]), bf16_hi(pw[w + 1]));
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+#pragma unroll
+            for (int i = 0; i < kKeys / 16; ++i)
+                tmem_st8_nowait(sbuf + 8 * i, pw[8 * i], pw[8 * i + 1], pw[8 * i + 2], pw[8 * i + 3], pw[8 * i + 4],
+                                pw[8 * i + 5], pw[8 * i + 6], pw[8 * i + 7]);
+            tmem_wait_st();
             if (t == 0 && k0 + kKeys > L) {
                 // keys at or past the sequence end: zero their V rows, whatever the slots hold
                 // (P is 0 there, but 0 times a NaN left in a slot is NaN).  Once V(j) has landed,
@@ -576,21 +482,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                     ok = false;
                     break;
                 }
-                uint8_t* vt = smem + kOffV + s * kTileBytes;
+                uint8_t* vt = smem + kOffV + s * kKVStage;
                 const int z0 = max(0, L - k0);
                 const int nchunks = (kKeys - z0) * 16;  // 16-byte chunks over both column halves
                 for (int c = r; c < nchunks; c += kRows) {
                     const int row = z0 + (c >> 4), half = (c >> 3) & 1, cc = c & 7;
-                    *reinterpret_cast<uint4*>(vt + half * kHalfBytes + row * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(vt + half * kKVHalf + row * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
             }
             tc_fence_before();
-            mbar_arrive(&bars->p_full[t]);
+            mbar_arrive(&bars->p_full[t][j & 1]);
         }
         if (nt > 0) {
-            if (ok) ok = !__any_sync(0xffffffffu, !mbar_wait(&bars->o_done[t], (nt - 1) & 1));
-            // one verdict for the warpgroup, which then takes the same path through its barriers
+            if (ok) ok = !__any_sync(0xffffffffu, !mbar_wait(&bars->o_final[t], 0));
+            // one verdict for the warpgroup, which then takes the same path
             const bool all_ok = named_sync_all(bar_id, 128, ok);
             if (all_ok) {
                 tc_fence_after();
@@ -631,8 +537,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
 
 cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
     static OncePerDevice configured;
-    const cudaError_t e = configured.run(
-        [] { return cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes); });
+    const cudaError_t e = configured.run([] {
+        // the register split is sound only at the launch count it was sized for
+        cudaFuncAttributes fa;
+        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_tc2_kernel);
+        if (r != cudaSuccess) return r;
+        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+        return cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
     if (e != cudaSuccess) return e;
     const int g = a.num_heads / pool.num_kv_heads;
     const int tpt = kRows / g;

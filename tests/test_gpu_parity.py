@@ -511,6 +511,22 @@ def test_prefill_whole_sequence_chunks():
     check_status_clean("whole-sequence chunks")
 
 
+@pytest.mark.parametrize("hq", [32, 64])
+def test_prefill_row_limits_at_stage_ends(hq):
+    """Rows whose causal limit falls exactly on the last key of a 64-key stage, or one past
+    it, inside a warp whose other rows see fewer keys (group 4: 8 queries to a warp, group 8:
+    4).  Every such warp must take the masked path together: a lane whose own limit alone
+    reads "the whole stage" may not branch away from its warp's collective tensor-memory
+    accesses.  Chunk lengths 33-40 over sequence ends 141-148 put rows on every stage end."""
+    lens = [141, 142, 144, 147, 148, 129, 192, 193]
+    qls = [33, 34, 36, 39, 40, 33, 64, 65]
+    case = W.paged_case(name="stage_ends", seed=5604, seq_lens=lens, q_lens=qls, new_lens=qls, num_heads=hq,
+                        num_kv_heads=8, head_dim=128, num_blocks=160)
+    g = GpuCase(case)
+    compare(g.prefill(), oracle_prefill(case), f"rows at stage ends, {hq} heads")
+    check_status_clean("rows at stage ends")
+
+
 def test_prefill_group16_and_oversized_max_chunk():
     """Group 16 on the tensor-core prefill (8 queries per 128-row tile), and a max_chunk far
     above the longest chunk (the grid is sized for it; the extra tiles have no rows)."""
