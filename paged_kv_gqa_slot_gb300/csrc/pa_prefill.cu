@@ -194,17 +194,18 @@ cudaError_t launch_prefill(const PoolView& pool, const AttnArgs& a, cudaStream_t
     const int g = a.num_heads / pool.num_kv_heads;
     // A chunk of a few queries (a speculative-decoding verify, one decode token) is a
     // bandwidth-bound decode with a causal mask: it runs on the decode kernel, its
-    // (query, head) rows on the MMA N dimension.  PA_PREFILL_IMPL=t or m forces the
-    // tensor-core or warp-MMA prefill kernels instead, for A/B comparisons; 2 selects the
-    // tensor-core kernel with 128-key stages.
+    // (query, head) rows on the MMA N dimension.  Longer chunks run on the tensor-core
+    // kernel with scores and P in tensor memory (pa_prefill_tc2.cu).  PA_PREFILL_IMPL forces a
+    // kernel for A/B comparisons: 2 that one, t the tensor-core kernel with Q in tensor memory
+    // and P in shared memory (pa_prefill_tc.cu), m the warp-MMA kernel.
     static const char forced = [] {
         const char* e = std::getenv("PA_PREFILL_IMPL");
         return e ? e[0] : '\0';
     }();
     if (forced != 't' && forced != 'm' && forced != '2' && decode_mq_supported(g, a.max_chunk))
         return launch_decode_mq(pool, a, stream);
-    if (prefill_tc_supported(pool.head_dim, g))
-        return forced == '2' ? launch_prefill_tc2(pool, a, stream) : launch_prefill_tc(pool, a, stream);
+    if (forced != 'm' && prefill_tc_supported(pool.head_dim, g))
+        return forced == 't' ? launch_prefill_tc(pool, a, stream) : launch_prefill_tc2(pool, a, stream);
     if (pool.head_dim == 128) return launch_mma<128>(pool, a, stream);
     return launch_mma<64>(pool, a, stream);
 }

@@ -109,6 +109,60 @@ __device__ __forceinline__ int pair_key_count(int p, int T, int tpt, int C, int 
     return max(tile_key_count(t0, tpt, C, L), tile_key_count(t1, tpt, C, L));
 }
 
+// Score c of a 64-key stage held in two 32-column loads.
+__device__ __forceinline__ float score(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int c) {
+    return __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+}
+
+// Maximum of the row's visible raw scores in one stage: keys c <= lim, or every key (kAll: a
+// stage wholly below the diagonal, the common case, needs no mask).  Four independent chains
+// of three-input max: one row per thread leaves no other parallelism to hide a long chain.
+template <bool kAll>
+__device__ __forceinline__ float stage_max(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int lim) {
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < kKeys; c += 2) {
+        float a0 = score(s0, s1, c), a1 = score(s0, s1, c + 1);
+        if (!kAll) {
+            a0 = c > lim ? -INFINITY : a0;
+            a1 = c + 1 > lim ? -INFINITY : a1;
+        }
+        m[(c >> 1) & 3] = fmax3(m[(c >> 1) & 3], a0, a1);
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// The row of P for one stage: p = 2^(s |scale| log2(e) - base) for keys c <= lim (every key
+// when kAll), one packed multiply-add per two keys and the special-function unit, rounded to
+// bf16 and stored as the row's 128 bytes of the 128-byte-swizzled P tile.  Returns the sum of
+// the rounded values (so the weights P V uses sum to the normaliser), in independent chains.
+template <bool kAll>
+__device__ __forceinline__ float stage_p(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int lim, float sl,
+                                         float nbase, uint8_t* prow, int r) {
+    float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int cc = 0; cc < kKeys / 8; ++cc) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const int c = cc * 8 + e;
+            float x0, x1;
+            fma_x2(x0, x1, score(s0, s1, c), score(s0, s1, c + 1), sl, sl, nbase, nbase);
+            if (!kAll) {
+                x0 = c > lim ? -INFINITY : x0;  // 2^-inf = 0
+                x1 = c + 1 > lim ? -INFINITY : x1;
+            }
+            w[e / 2] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
+        }
+        add_x2(ls[0], ls[1], bf16_lo(w[0]), bf16_hi(w[0]));
+        add_x2(ls[2], ls[3], bf16_lo(w[1]), bf16_hi(w[1]));
+        add_x2(ls[4], ls[5], bf16_lo(w[2]), bf16_hi(w[2]));
+        add_x2(ls[6], ls[7], bf16_lo(w[3]), bf16_hi(w[3]));
+        *reinterpret_cast<uint4*>(prow + swz128(r, cc)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+}
+
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                  const __grid_constant__ CUtensorMap tm_v,
                                                                  const __grid_constant__ TcArgs a) {
@@ -347,29 +401,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
             const int k0 = j * kKeys;
             const int lim = pos - k0;  // keys c <= lim of this tile are visible to the row
-            float sv[kKeys];
-#pragma unroll
-            for (int c = 0; c < kKeys; ++c) sv[c] = __uint_as_float(sr[c >> 5][c & 31]);
-            // Row maximum of the raw scores (|scale| keeps the order), in independent chains:
-            // one row per thread leaves no other parallelism to hide a long dependent chain.
-            // Tiles wholly below the diagonal need no mask; only they are common.
-            float mx;
-            if (lim >= kKeys - 1) {
-                float m4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) m4[e] = fmaxf(sv[2 * e], sv[2 * e + 1]);
-#pragma unroll
-                for (int c = 8; c < kKeys; c += 8) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) m4[e] = fmax3(m4[e], sv[c + 2 * e], sv[c + 2 * e + 1]);
-                }
-                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            } else {
-                mx = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < kKeys; ++c)
-                    if (c <= lim) mx = fmaxf(mx, sv[c]);
-            }
+            // Tiles wholly below the diagonal (every row of the warp sees all 64 keys) take the
+            // path without a mask; only they are common.  The warp's vote picks the path, so
+            // the warp stays converged through the collective accesses below.
+            const bool unmasked = __all_sync(0xffffffffu, lim >= kKeys - 1);
+            const float mx = unmasked ? stage_max<true>(sr[0], sr[1], lim) : stage_max<false>(sr[0], sr[1], lim);
             const float mxs = mx == -INFINITY ? -INFINITY : mx * a.scale_log2;  // log2 units
             const float m_new = fmaxf(m_used, mxs);
             const bool rescale = m_new > m_used + kRescaleThreshold;  // always for the first visible key
@@ -406,40 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
             }
             const float nbase = m_used == -INFINITY ? 0.f : -m_used;
             uint8_t* prow = smem + kOffP + (t * kPBufs + pb) * kPBytes;
-            // p = 2^(s |scale| log2(e) - m): one packed multiply-add per two keys, then the
-            // special-function unit; P is rounded to bf16 for P V, and the row sum adds those
-            // rounded values (in four packed chains), so the weights P V uses sum to l.
-            float ls[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) ls[e] = 0.f;
-            const bool masked = lim < kKeys - 1;
-#pragma unroll
-            for (int cc = 0; cc < kKeys / 8; ++cc) {
-                float pp[8];
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    float x0, x1;
-                    fma_x2(x0, x1, sv[cc * 8 + e], sv[cc * 8 + e + 1], a.scale_log2, a.scale_log2, nbase, nbase);
-                    pp[e] = fast_exp2(x0);
-                    pp[e + 1] = fast_exp2(x1);
-                }
-                if (masked) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        if (cc * 8 + e > lim) pp[e] = 0.f;
-                }
-                uint4 v;
-                v.x = pack_bf16x2(pp[0], pp[1]);
-                v.y = pack_bf16x2(pp[2], pp[3]);
-                v.z = pack_bf16x2(pp[4], pp[5]);
-                v.w = pack_bf16x2(pp[6], pp[7]);
-                add_x2(ls[0], ls[1], bf16_lo(v.x), bf16_hi(v.x));
-                add_x2(ls[2], ls[3], bf16_lo(v.y), bf16_hi(v.y));
-                add_x2(ls[4], ls[5], bf16_lo(v.z), bf16_hi(v.z));
-                add_x2(ls[6], ls[7], bf16_lo(v.w), bf16_hi(v.w));
-                *reinterpret_cast<uint4*>(prow + swz128(r, cc)) = v;
-            }
-            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            l += unmasked ? stage_p<true>(sr[0], sr[1], lim, a.scale_log2, nbase, prow, r)
+                          : stage_p<false>(sr[0], sr[1], lim, a.scale_log2, nbase, prow, r);
             if (k0 + kKeys > L && j >= zero_from) {
                 // keys at or past the sequence end: zero their V rows, whatever the slots hold.
                 // Once V(j) has landed, every earlier reader of the slot has finished (its

@@ -19,15 +19,16 @@
 // Tensor memory: tile t owns columns [256t, 256t+256): two 64-column score buffers, stage j
 // in buffer j % 2, and O_t [128, 256).  So S_t(j+1) is computed while the softmax works on
 // stage j, and P_t V(j) only gates S_t(j+2), which reuses the buffer P_t(j) sits in: the
-// tensor core runs the MMAs of one CTA in issue order, and the MMA warp issues, per stage j
-// and tile t, P_t V(j) then S_t(j+2).  The two tiles' softmax warpgroups run side by side.
+// tensor core runs one issuer's MMAs in order, and tile t's MMA warp issues, per stage j,
+// P_t V(j) then S_t(j+2).  Each tile has its own MMA warp, so a tile waiting for its P never
+// holds up the other's MMAs; the two tiles' softmax warpgroups run side by side.
 // The running max is re-based lazily: O is rescaled in TMEM only when a row's max grows by
 // more than 2^8, which keeps every P <= 256 and makes rescales rare.
 // Q tiles come in by TMA through a 3-D map of q (d, head, token) whose box is one tile (a tile
 // cut short by the end of its chunk row by row instead); each row of O is stored by its thread.
 // Warp roles: 0-3 softmax of tile 0, 4-7 softmax of tile 1 (TMEM lanes 32(w%4)..+31),
-// 8 MMA issue + TMEM owner, 9 TMA loads of K, 10 TMA loads of V, 11 idle (it completes the
-// control warpgroup, which hands registers to the softmax warpgroups).  Every CTA loads its
+// 8 MMA issue of tile 0 + TMEM owner, 9 TMA loads of K, 10 TMA loads of V, 11 MMA issue of
+// tile 1; this control warpgroup hands registers to the softmax warpgroups.  Every CTA loads its
 // own K/V; the CTAs of one (sequence, kv head) -- and, with a shared prefix, of every
 // sequence that shares it -- read the same pool blocks, the copies after the first from L2.
 #include <algorithm>
@@ -46,8 +47,11 @@ constexpr int kTiles = 2;                       // query tiles per CTA
 constexpr int kKeys = 64;                       // keys per stage (MMA N of S, K of P V)
 constexpr int kKStages = 4, kVStages = 4;       // K and V ring slots
 constexpr int kSoftmaxThreads = kTiles * 128;
-constexpr int kMmaWarp = kSoftmaxThreads / 32, kKLoadWarp = kMmaWarp + 1, kVLoadWarp = kMmaWarp + 2;
-constexpr int kThreads = kSoftmaxThreads + 128;   // + a control warpgroup: MMA, K, V, idle
+// control warpgroup: MMA issue for tile 0 (and TMEM owner), TMA loads of K, of V, MMA issue for tile 1
+constexpr int kMmaWarp = kSoftmaxThreads / 32, kKLoadWarp = kMmaWarp + 1, kVLoadWarp = kMmaWarp + 2,
+              kMmaWarp1 = kMmaWarp + 3;
+constexpr int kThreads = kSoftmaxThreads + 128;
+static_assert(kMmaWarp1 == kThreads / 32 - 1, "warp roles");
 // Registers: launched at kLaunchRegs a thread (65536 / 384 threads), the control warpgroup
 // gives some back and the softmax warpgroups take them (setmaxnreg); the shares add up to
 // exactly the launch's total, and the launcher checks the compiled count.
@@ -64,20 +68,23 @@ constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTiles * kQTile;
 constexpr int kOffV = kOffK + kKStages * kKVStage;
 constexpr int kBarOff = kOffV + kVStages * kKVStage;
-constexpr int kSmemBytes = kBarOff + 256 + 1024;
+constexpr int kSmemBytes = kBarOff + 512 + 1024;
 constexpr float kRescaleThreshold = 8.f;        // log2 units
 constexpr float kLog2e = 1.44269504088896340736f;
 
 struct Bars {
-    uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    // a ring slot is refilled once each tile that reads it has released it (the tiles' MMAs
+    // are issued by different warps, so each commits its own release)
+    uint64_t k_full[kKStages], k_empty[kTiles][kKStages], v_full[kVStages], v_empty[kTiles][kVStages];
     // per tile: scores and P of stage j use buffer j % 2 (a softmax may finish two stages before
     // the MMA warp waits for the first, so one barrier per buffer keeps their phases apart);
     // o_done completes after every P V, o_final after the tile's last one
     uint64_t q_full[kTiles], s_full[kTiles][2], p_full[kTiles][2], o_done[kTiles], o_final[kTiles];
-    uint64_t drain;
+    uint64_t drain[kTiles];
+    uint64_t v_zero;  // tile 0's softmax has zeroed the V rows past the sequence end
     uint32_t tmem_base;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 struct Tc2Args {
@@ -118,6 +125,47 @@ __device__ __forceinline__ bool named_sync_all(int id, int count, bool pred) {
         : "r"((uint32_t)pred), "r"(id), "r"(count)
         : "memory");
     return r != 0;
+}
+
+// Score c of a 64-key stage held in two 32-column loads.
+__device__ __forceinline__ float score(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int c) {
+    return __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+}
+
+// Maximum of the row's visible scores in one stage: keys c <= lim, or every key (kAll, a
+// stage wholly below the diagonal, which is the common case and needs no mask).  Four
+// independent chains of three-input max.
+template <bool kAll>
+__device__ __forceinline__ float stage_max(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int lim) {
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < kKeys; c += 2) {
+        float a0 = score(s0, s1, c), a1 = score(s0, s1, c + 1);
+        if (!kAll) {
+            a0 = c > lim ? -INFINITY : a0;
+            a1 = c + 1 > lim ? -INFINITY : a1;
+        }
+        m[(c >> 1) & 3] = fmax3(m[(c >> 1) & 3], a0, a1);
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// p = 2^(s scale log2(e) - base) for the stage's keys (0 for keys past lim unless kAll),
+// rounded to bf16 two keys to a 32-bit word, the layout P V reads from tensor memory: one
+// packed multiply-add per two keys, the special-function unit, bf16 packing.
+template <bool kAll>
+__device__ __forceinline__ void stage_exps(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int lim, float sl,
+                                           float nbase, uint32_t (&pw)[kKeys / 2]) {
+#pragma unroll
+    for (int c = 0; c < kKeys; c += 2) {
+        float x0, x1;
+        fma_x2(x0, x1, score(s0, s1, c), score(s0, s1, c + 1), sl, sl, nbase, nbase);
+        if (!kAll) {
+            x0 = c > lim ? -INFINITY : x0;  // 2^-inf = 0
+            x1 = c + 1 > lim ? -INFINITY : x1;
+        }
+        pw[c / 2] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
+    }
 }
 
 // O (the row's 128 fp32 columns of tensor memory at `taddr`) *= f, in 8-column pieces.
@@ -165,11 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
-            mbar_init(&bars->k_empty[s], 1);
+            for (int t = 0; t < kTiles; ++t) mbar_init(&bars->k_empty[t][s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars->v_full[s], 1);
-            mbar_init(&bars->v_empty[s], 1);
+            for (int t = 0; t < kTiles; ++t) mbar_init(&bars->v_empty[t][s], 1);
         }
         for (int t = 0; t < kTiles; ++t) {
             mbar_init(&bars->q_full[t], 1);
@@ -179,8 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
             mbar_init(&bars->p_full[t][1], 128);
             mbar_init(&bars->o_done[t], 1);
             mbar_init(&bars->o_final[t], 1);
+            mbar_init(&bars->drain[t], 1);
         }
-        mbar_init(&bars->drain, 1);
+        mbar_init(&bars->v_zero, 128);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -202,7 +251,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
             const bool is_k = warp == kKLoadWarp;
             const CUtensorMap* map = is_k ? &tm_k : &tm_v;
             uint64_t* full = is_k ? bars->k_full : bars->v_full;
-            uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+            uint64_t* empty0 = is_k ? bars->k_empty[0] : bars->v_empty[0];
+            uint64_t* empty1 = is_k ? bars->k_empty[1] : bars->v_empty[1];
             uint8_t* ring = smem + (is_k ? kOffK : kOffV);
             const int nslots = is_k ? kKStages : kVStages;
             if (lane == 0) prefetch_tensormap(map);
@@ -228,7 +278,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                 const int row = lb < nblk ? (id * a.num_kv_heads + kvh) * kBlockSize : oob_row;
                 const int s = j % nslots;
                 if (lane == 0) {
-                    if (j >= nslots) ok = mbar_wait(&empty[s], ((j / nslots) & 1) ^ 1);
+                    // the slot's previous stage, j - nslots, was read by tile 0 and, if it is one
+                    // of its stages, by tile 1
+                    if (j >= nslots) {
+                        const uint32_t par = ((j / nslots) & 1) ^ 1;
+                        ok = mbar_wait(&empty0[s], par);
+                        if (ok && j - nslots < nst[1]) ok = mbar_wait(&empty1[s], par);
+                    }
                     if (ok) mbar_arrive_expect_tx(&full[s], kKVStage);
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
@@ -245,83 +301,74 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                     if (!mbar_wait(&full[j % nslots], (j / nslots) & 1)) ok = false;
                 if (!ok) atomicOr(a.status, kDevTimeout);
             }
-        } else if (warp == kMmaWarp) {
-            // -------------------------------------------------------- MMA issue (whole warp)
-            // The warp runs the loop together and one elected lane issues, so every operand is
-            // warp-uniform; waits give one verdict for the warp.  Operand descriptors are built
-            // once; a tile, a stage or a k-step only moves the start address, which adds
-            // (offset >> 4) to the low field (no carry: every shared address is below 2^18).
+        } else {
+            // -------------------------------------------------------- MMA issue, one warp per tile
+            // Each tile's chain -- its P(j), then P V(j), then S(j+2) into the buffer P(j) held --
+            // runs in its own warp, so while one warp waits for its tile's P the other keeps the
+            // tensor core busy (a waiting issuer leaves it idle: issue runs only a few MMAs
+            // ahead of execution).  The warp runs the loop together and one elected lane issues,
+            // so every operand is warp-uniform; waits give one verdict for the warp.  Operand
+            // descriptors are built once; a stage or a k-step only moves the start address,
+            // which adds (offset >> 4) to the low field (no carry: every shared address is
+            // below 2^18).
+            const int t = warp == kMmaWarp1 ? 1 : 0;
+            const int n = nst[t];
+            // the one stage whose V rows past the sequence end tile 0's softmax zeroes (-1: none)
+            const int jz = kKeys * nst[0] > L ? nst[0] - 1 : -1;
             constexpr uint32_t idesc_s = tc_idesc_bf16(kRows, kKeys, false);
             constexpr uint32_t idesc_o = tc_idesc_bf16(kRows, kD, true);
-            const uint64_t qdesc0 = smem_desc_sw128(smem_u32(smem + kOffQ), 0, 1024);
+            const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + t * kQTile), 0, 1024);
             const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + kOffK), 0, 1024);
             const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + kOffV), kKVHalf, 1024);
-            auto issue_qk = [&](int t, int j) {  // S_t(j) = Q_t K(j)^T into score buffer j % 2
-                const uint64_t qd = qdesc0 + (uint64_t)((t * kQTile) >> 4);
+            const uint32_t tm_t = tmem + t * kTmemTile;
+            auto issue_qk = [&](int j) {  // S(j) = Q K(j)^T into score buffer j % 2
                 const uint64_t kd = kdesc0 + (uint64_t)(((j % kKStages) * kKVStage) >> 4);
-                const uint32_t tm_s = tmem + t * kTmemTile + kTmemS + 64 * (j & 1);
+                const uint32_t tm_s = tm_t + kTmemS + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     tc_mma_ew(tm_s, qd + (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
                               kd + (uint64_t)(((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idesc_s, kk > 0 ? 1u : 0u);
                 tc_commit_ew(&bars->s_full[t][j & 1]);
+                tc_commit_ew(&bars->k_empty[t][j % kKStages]);
             };
-            auto issue_pv = [&](int t, int j) {  // O_t += P_t(j) V(j), P_t(j) in score buffer j % 2
+            auto issue_pv = [&](int j) {  // O += P(j) V(j), P(j) in score buffer j % 2
                 const uint64_t vd = vdesc0 + (uint64_t)(((j % kVStages) * kKVStage) >> 4);
-                const uint32_t tm_p = tmem + t * kTmemTile + kTmemS + 64 * (j & 1);
-                const uint32_t tm_o = tmem + t * kTmemTile + kTmemO;
+                const uint32_t tm_p = tm_t + kTmemS + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk)
-                    tc_mma_ts_ew(tm_o, tm_p + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                    tc_mma_ts_ew(tm_t + kTmemO, tm_p + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                  (j > 0 || kk > 0) ? 1u : 0u);
                 tc_commit_ew(&bars->o_done[t]);
-                if (j + 1 == nst[t]) tc_commit_ew(&bars->o_final[t]);
+                tc_commit_ew(&bars->v_empty[t][j % kVStages]);
+                if (j + 1 == n) tc_commit_ew(&bars->o_final[t]);
             };
             bool ok = true;
-#pragma unroll
-            for (int t = 0; t < kTiles; ++t)
-                if (ok && nst[t] > 0) ok = mbar_wait_warp(&bars->q_full[t], 0);
-            // stages 0 and 1 of both tiles into the two score buffers
-            for (int j = 0; j < 2 && j < nstage && ok; ++j) {
+            if (n > 0) ok = mbar_wait_warp(&bars->q_full[t], 0);
+            // stages 0 and 1 into the two score buffers
+            for (int j = 0; j < 2 && j < n && ok; ++j) {
                 ok = mbar_wait_warp(&bars->k_full[j], 0);
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
-                for (int t = 0; t < kTiles; ++t)
-                    if (j < nst[t]) issue_qk(t, j);
-                tc_commit_ew(&bars->k_empty[j]);  // K(j) is read by S(j) of both tiles only
+                issue_qk(j);
             }
-            for (int j = 0; j < nstage && ok; ++j) {
-                bool v_ready = false, k_ready = false;
-#pragma unroll
-                for (int t = 0; t < kTiles; ++t) {
-                    if (!ok || j >= nst[t]) continue;
-                    ok = mbar_wait_warp(&bars->p_full[t][j & 1], (j >> 1) & 1);
-                    if (ok && !v_ready) {
-                        ok = mbar_wait_warp(&bars->v_full[j % kVStages], (j / kVStages) & 1);
-                        v_ready = true;
-                    }
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(t, j);
-                    if (j + 2 < nst[t]) {
-                        // S_t(j+2) reuses the buffer P_t(j) sits in: after P_t V(j) in issue order
-                        if (!k_ready) {
-                            ok = mbar_wait_warp(&bars->k_full[(j + 2) % kKStages], ((j + 2) / kKStages) & 1);
-                            k_ready = true;
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        issue_qk(t, j + 2);
-                    }
-                }
+            for (int j = 0; j < n && ok; ++j) {
+                // The operands the stage needs besides P -- V(j), K(j+2) and, for tile 1, the
+                // zeroed tail of V -- are waited for first (they are normally long in place),
+                // so that once P(j) is complete P V(j) and S(j+2) go out back to back.
+                ok = mbar_wait_warp(&bars->v_full[j % kVStages], (j / kVStages) & 1);
+                if (ok && j + 2 < n) ok = mbar_wait_warp(&bars->k_full[(j + 2) % kKStages], ((j + 2) / kKStages) & 1);
+                // tile 1 reads the zeroed rows only once tile 0's softmax has written them
+                if (ok && t == 1 && j == jz) ok = mbar_wait_warp(&bars->v_zero, 0);
+                if (ok) ok = mbar_wait_warp(&bars->p_full[t][j & 1], (j >> 1) & 1);
                 if (!ok) break;
-                tc_commit_ew(&bars->v_empty[j % kVStages]);
-                if (k_ready) tc_commit_ew(&bars->k_empty[(j + 2) % kKStages]);
+                tc_fence_after();
+                issue_pv(j);
+                // S(j+2) reuses the buffer P(j) sits in: after P V(j) in this warp's issue order
+                if (j + 2 < n) issue_qk(j + 2);
             }
-            // every MMA issued above has finished before the tensor memory is released
-            tc_commit_ew(&bars->drain);
-            if (!mbar_wait_warp(&bars->drain, 0)) ok = false;
+            // every MMA this warp issued has finished before the tensor memory is released
+            tc_commit_ew(&bars->drain[t]);
+            if (!mbar_wait_warp(&bars->drain[t], 0)) ok = false;
             if (!ok && lane == 0) atomicOr(a.status, kDevTimeout);
         }
     } else {
@@ -332,7 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         const int mt = t == 0 ? mtile[0] : mtile[1], nt = t == 0 ? nst[0] : nst[1];
         const int tok0 = mt * tpt;
         const int ntok = (mt >= 0 && tok0 < C) ? min(tpt, C - tok0) : 0;
-        const bool whole = ntok == tpt;             // the tile is whole: Q comes in by TMA
+        // A negative scale enters as -Q (exact in bf16) against |scale|, so the row maximum is
+        // always taken over the scores as they are; such Q is negated on the way in, by threads.
+        const bool neg = a.scale_log2 < 0.f;
+        const bool whole = ntok == tpt && !neg;     // a whole tile at a positive scale: Q by TMA
         const bool valid = r < ntok * g;
         const int qi = r / g, h = r % g;
         const int pos = valid ? L - C + tok0 + qi : -1;  // causal limit of the row (inclusive)
@@ -349,23 +399,28 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                     tma_load_3d(qs + kQHalf, &tm_q, 64, kvh * g, q0 + tok0, &bars->q_full[t]);
                 }
             } else {
-                // row by row into the same 128-byte swizzled layout (zeros past the chunk)
+                // row by row into the same 128-byte swizzled layout (zeros past the chunk); the
+                // sign bit of every bf16 flips for a negative scale
                 const uint4* src = reinterpret_cast<const uint4*>(
                     a.q + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD);
+                const uint32_t flip = neg ? 0x80008000u : 0u;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-                    for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<uint4*>(qs + hh * kQHalf + swz128(r, c)) =
-                            valid ? __ldg(src + hh * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 v = valid ? __ldg(src + hh * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+                        v.x ^= flip;
+                        v.y ^= flip;
+                        v.z ^= flip;
+                        v.w ^= flip;
+                        *reinterpret_cast<uint4*>(qs + hh * kQHalf + swz128(r, c)) = v;
+                    }
                 fence_proxy_async_smem();
                 named_sync(bar_id, 128);
                 if (r == 0) mbar_arrive(&bars->q_full[t]);
             }
         }
-        const float sl = a.scale_log2;
-        const float sl_abs = fabsf(sl);
-        const bool neg = sl < 0.f;  // the row maximum of scale * s is scale * min(s) then
+        const float sl = fabsf(a.scale_log2);  // Q carries the sign
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         // tcgen05.ld / tcgen05.st are warp-collective: every decision that leads to one (a wait
@@ -379,85 +434,41 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
             tc_fence_after();
             const int k0 = j * kKeys;
             const int lim = pos - k0;  // keys c <= lim of this stage are visible to the row
-            // Stages wholly below the diagonal (every row of the warp sees all 64 keys) need no
-            // mask; only they are common.  The choice of path below rests on the vote alone: a
-            // row whose own limit happens to be 64 must not take the unmasked path by itself.
+            // Stages wholly below the diagonal (every row of the warp sees all 64 keys) take the
+            // path without a mask; only they are common.  The path is the warp's vote, never a
+            // row's own limit: the branches below hold warp-collective tensor-memory accesses.
             const bool unmasked = __all_sync(0xffffffffu, lim >= kKeys - 1);
-            const int mlim = unmasked ? kKeys : lim;
-            // p = 2^(s scale log2(e) - m), rounded to bf16, two keys to a 32-bit word (the layout
-            // P V reads from tensor memory): one packed multiply-add per two keys, the
-            // special-function unit, bf16 packing
-            uint32_t pw[kKeys / 2];
-            auto exps = [&](int c, const uint32_t (&sr)[32], float nbase) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const int kb = c * 32 + e;
-                    float x0, x1, x2, x3;
-                    fma_x2(x0, x1, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]), sl, sl, nbase, nbase);
-                    fma_x2(x2, x3, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]), sl, sl, nbase, nbase);
-                    float e0 = fast_exp2(x0), e1 = fast_exp2(x1), e2 = fast_exp2(x2), e3 = fast_exp2(x3);
-                    e0 = kb > mlim ? 0.f : e0;
-                    e1 = kb + 1 > mlim ? 0.f : e1;
-                    e2 = kb + 2 > mlim ? 0.f : e2;
-                    e3 = kb + 3 > mlim ? 0.f : e3;
-                    pw[kb / 2] = pack_bf16x2(e0, e1);
-                    pw[kb / 2 + 1] = pack_bf16x2(e2, e3);
-                }
-            };
-            // row maximum of the sign-adjusted scores over keys <= mlim (|scale| keeps the order
-            // of s, or reverses it for a negative scale, where it is taken over -s), 4 chains
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            auto maxs = [&](int c, const uint32_t (&sr)[32]) {
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const int kb = c * 32 + e;
-                    float a0 = __uint_as_float(sr[e]), a1 = __uint_as_float(sr[e + 1]);
-                    a0 = kb > mlim ? -INFINITY : (neg ? -a0 : a0);
-                    a1 = kb + 1 > mlim ? -INFINITY : (neg ? -a1 : a1);
-                    m4[(e >> 1) & 3] = fmax3(m4[(e >> 1) & 3], a0, a1);
-                }
-            };
             uint32_t s0[32], s1[32];
             tmem_ld32_async(sbuf, s0);
             tmem_ld32_async(sbuf + 32, s1);
             tmem_wait_ld(s0);
             tmem_wait_ld(s1);
-            // Below the diagonal after the first stage, the exponentials go against the running
-            // base beside the maximum; a row whose maximum outgrows the base does them again
-            // with the new one (computing them against the old one and rescaling would round
-            // them twice).  Elsewhere the maximum comes first.
-            const bool spec = j > 0 && unmasked;  // warp-uniform: the branches below are collective
-            if (spec) {
-                exps(0, s0, -m_used);
-                exps(1, s1, -m_used);
-            }
-            maxs(0, s0);
-            maxs(1, s1);
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            const float mxs = mx == -INFINITY ? -INFINITY : mx * sl_abs;  // log2 units
+            const float mx = unmasked ? stage_max<true>(s0, s1, lim) : stage_max<false>(s0, s1, lim);
+            const float mxs = mx == -INFINITY ? -INFINITY : mx * sl;  // log2 units
             const float m_new = fmaxf(m_used, mxs);
             const bool rebase = m_new > m_used + kRescaleThreshold;  // always for the first visible key
-            if (__any_sync(0xffffffffu, rebase) || !spec) {
-                if (__any_sync(0xffffffffu, rebase && m_used != -INFINITY)) {
-                    // O_t changes only once P_t V(j-1) -- which may still run, since S_t(j) was
-                    // ready long before -- has finished: its commit is o_done phase j-1 (phases
-                    // up to j-2 are complete, as S_t(j) was issued after P_t V(j-2), and P_t V(j)
-                    // waits for this stage's P, so the parity cannot alias)
-                    if (j > 0 && __any_sync(0xffffffffu, !mbar_wait(&bars->o_done[t], (j - 1) & 1))) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    scale_o(tm_row + kTmemO, rebase && m_used != -INFINITY ? fast_exp2(m_used - m_new) : 1.f);
+            if (__any_sync(0xffffffffu, rebase && m_used != -INFINITY)) {
+                // O_t changes only once P_t V(j-1) -- which may still run, since S_t(j) was
+                // ready long before -- has finished: its commit is o_done phase j-1 (phases up
+                // to j-2 are complete, as S_t(j) was issued after P_t V(j-2), and P_t V(j) waits
+                // for this stage's P, so the parity cannot alias)
+                if (j > 0 && __any_sync(0xffffffffu, !mbar_wait(&bars->o_done[t], (j - 1) & 1))) {
+                    ok = false;
+                    break;
                 }
-                if (rebase) {
-                    l *= m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
-                    m_used = m_new;
-                }
-                const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-                exps(0, s0, nbase);
-                exps(1, s1, nbase);
+                tc_fence_after();
+                scale_o(tm_row + kTmemO, rebase && m_used != -INFINITY ? fast_exp2(m_used - m_new) : 1.f);
             }
+            if (rebase) {
+                l *= m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
+                m_used = m_new;
+            }
+            const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+            uint32_t pw[kKeys / 2];
+            if (unmasked)
+                stage_exps<true>(s0, s1, lim, sl, nbase, pw);
+            else
+                stage_exps<false>(s0, s1, lim, sl, nbase, pw);
             // The row sum adds the rounded values, so the weights P V uses sum to l; then P goes
             // over the first 32 columns of the stage's buffer.
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
@@ -475,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
             if (t == 0 && k0 + kKeys > L) {
                 // keys at or past the sequence end: zero their V rows, whatever the slots hold
                 // (P is 0 there, but 0 times a NaN left in a slot is NaN).  Once V(j) has landed,
-                // its slot's previous readers have finished (the refill waited for them), and
-                // both tiles' P V(j) are issued after tile 0's P(j) is complete.
+                // its slot's previous readers have finished (the refill waited for them); tile
+                // 0's P V(j) follows its P(j), and tile 1's waits for the v_zero arrival below.
                 const int s = j % kVStages;
                 if (__any_sync(0xffffffffu, !mbar_wait(&bars->v_full[s], (j / kVStages) & 1))) {
                     ok = false;
@@ -490,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                     *reinterpret_cast<uint4*>(vt + half * kKVHalf + row * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
+                mbar_arrive(&bars->v_zero);  // tile 1's P V of this stage waits for it
             }
             tc_fence_before();
             mbar_arrive(&bars->p_full[t][j & 1]);

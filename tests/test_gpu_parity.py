@@ -630,3 +630,48 @@ def test_concurrent_first_calls_from_threads(tmp_path):
     root = str(Path(__file__).resolve().parents[1])
     r = subprocess.run([sys.executable, str(script), root], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
+
+
+_ALTERNATE_PREFILL = r'''
+import sys
+import torch
+sys.path[:0] = [sys.argv[1], sys.argv[1] + "/tests"]
+import workloads as W
+from parity import GpuCase, compare, oracle_prefill, check_status_clean
+cases = [
+    W.chunked_prefill(seed=1105, batch=3, prefix_blocks=5, chunk=100),
+    W.random_case(5901, batch=4, num_heads=32, num_kv_heads=8, head_dim=128, min_len=1, max_len=200, q_len=70,
+                  prefill=True, shared_prefix_tokens=32),
+    W.paged_case(name="stage_ends", seed=5604, seq_lens=[141, 142, 144, 147, 148, 129, 192, 193],
+                 q_lens=[33, 34, 36, 39, 40, 33, 64, 65], new_lens=[33, 34, 36, 39, 40, 33, 64, 65],
+                 num_heads=32, num_kv_heads=8, head_dim=128, num_blocks=160),
+    W.random_case(5902, batch=3, num_heads=16, num_kv_heads=4, head_dim=128, min_len=1, max_len=180, q_len=40,
+                  prefill=True, shared_prefix_tokens=16, scale=-0.09),
+    W.random_case(5903, batch=3, num_heads=64, num_kv_heads=4, head_dim=128, min_len=40, max_len=400, q_len=150,
+                  prefill=True, shared_prefix_tokens=16),
+]
+for i, c in enumerate(cases):
+    compare(GpuCase(c).prefill(), oracle_prefill(c), f"{sys.argv[2]} prefill case {i}")
+    check_status_clean(f"{sys.argv[2]} prefill case {i}")
+print("ok")
+'''
+
+
+@pytest.mark.parametrize("impl", ["t", "m"])
+def test_alternate_prefill_kernels(impl, tmp_path):
+    """The prefill kernels the default path does not pick for these shapes, forced by
+    PA_PREFILL_IMPL in a child process (the choice is read once per process): t, the
+    tensor-core kernel with Q in tensor memory and P in shared memory; m, the warp-MMA
+    kernel.  Ragged chunks, rows on stage ends, a negative scale and group 16, against the
+    oracle."""
+    import os
+    import subprocess
+    import sys
+    from pathlib import Path
+    script = tmp_path / "pa_alternate_prefill.py"
+    script.write_text(_ALTERNATE_PREFILL)
+    root = str(Path(__file__).resolve().parents[1])
+    env = dict(os.environ, PA_PREFILL_IMPL=impl)
+    r = subprocess.run([sys.executable, str(script), root, impl], capture_output=True, text=True, timeout=600,
+                       env=env)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
