@@ -689,14 +689,17 @@ class OracleSample:
     """A bounded sample of the decode step for the fp64 CPU oracle: the append + decode of the
     first `decode_seqs` batched-decode sequences and both split-KV workloads with their merge;
     with `prefill_stride`, also the chunked prefill on every prefill_stride-th (token, head)
-    row (the full-path sample)."""
+    row (the full-path sample).  `parts` are the split-KV partition counts of the two
+    workloads: the step's own, or 16 for both (the library's count for these shapes on 152
+    SMs) where no GPU is there to ask."""
 
-    def __init__(self, decode_seqs=None, prefill_stride=None):
+    def __init__(self, decode_seqs=None, prefill_stride=None, parts=(16, 16)):
         import oracle
         import workloads as W
         from workloads import u16
         self.orc = oracle.load()
         self.u16 = u16
+        self.parts = tuple(int(p) for p in parts)
         self.c3 = W.batched_decode()
         if decode_seqs is not None:
             self.c3 = self._first_seqs(self.c3, decode_seqs)
@@ -733,7 +736,7 @@ class OracleSample:
         c = self.c3
         o.kv_append(k, v, u16(c.k_new), u16(c.v_new), c.slot_mapping.numpy())
         o.decode(k, v, u16(c.q), c.block_tables.numpy(), c.seq_lens.numpy(), c.scale)
-        for name, c, P in (("c4a", self.c4a, 19), ("c4b", self.c4b, 32)):
+        for name, c, P in (("c4a", self.c4a, self.parts[0]), ("c4b", self.c4b, self.parts[1])):
             k, v = self.pools[name]
             op, lse = o.decode_partitions(k, v, u16(c.q), c.block_tables.numpy(), c.seq_lens.numpy(), c.scale, P)
             o.combine(op, lse)
@@ -745,8 +748,8 @@ class OracleSample:
                            self.rows_t, self.rows_h)
 
     def describe(self) -> str:
-        s = (f"append + decode of {self.c3.batch} batched-decode sequences, split-KV 4x8192 (P=19) and 1x32768 "
-             f"(P=32) with their merge")
+        s = (f"append + decode of {self.c3.batch} batched-decode sequences, split-KV 4x8192 (P={self.parts[0]}) and "
+             f"1x32768 (P={self.parts[1]}) with their merge")
         if self.c5 is not None:
             s += f", append + chunked prefill on {self.prefill_frac:.4f} of its (token, head) rows"
         return s + f"; {self.kv_bytes / 1e6:.1f} MB of KV"
@@ -943,7 +946,7 @@ def main(argv=None):
 
     cpu = None
     if rank == 0 and ws == 1 and extras and not args.no_cpu_baseline:
-        sample = OracleSample(decode_seqs=16)
+        sample = OracleSample(decode_seqs=16, parts=(step.P4a, step.P4b))
         v1, dt1, _ = sample.time(1)
         vall, dtall, used = sample.time(os.cpu_count() or 1, reps=3)
         cpu = {"value": round(vall, 4), "unit": "GB/s", "cores": used, "kind": "oracle",

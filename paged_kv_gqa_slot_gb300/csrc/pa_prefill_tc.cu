@@ -503,12 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 }  // namespace
 
 bool prefill_tc_supported(int head_dim, int group) {
-    if (head_dim != kD || group <= 0 || group > kRows || kRows % group != 0) return false;
-    static const bool disabled = [] {
-        const char* e = std::getenv("PA_PREFILL_IMPL");
-        return e && e[0] == 'm';  // "mma": the warp-MMA kernel, for A/B comparisons
-    }();
-    return !disabled;
+    return head_dim == kD && group > 0 && group <= kRows && kRows % group == 0;
 }
 
 cudaError_t launch_prefill_tc(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
