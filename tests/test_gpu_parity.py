@@ -224,6 +224,21 @@ def test_prefill_ragged_sweep(hq, hkv, d):
     check_status_clean("prefill sweep")
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (16, 8), (32, 8), (64, 8), (64, 4), (64, 2)],
+                         ids=["g1", "g2", "g4", "g8", "g16", "g32"])
+def test_prefill_group_sweep(hq, hkv):
+    """Every group size the tensor-core prefill takes from 1 to 32 (128 to 4 queries a tile),
+    chunks of up to 300 queries over sequences of up to 700 tokens -- several query tiles, odd
+    tile counts (a pair with one tile), ragged last tiles and sequence ends inside a stage --
+    without and with a 48-token shared prefix."""
+    for j, shared in enumerate((0, 48)):
+        case = W.random_case(5400 + hq + 3 * hkv + j, batch=4, num_heads=hq, num_kv_heads=hkv, head_dim=128,
+                             min_len=1 + shared, max_len=700, q_len=300, prefill=True, shared_prefix_tokens=shared)
+        g = GpuCase(case)
+        compare(g.prefill(), oracle_prefill(case), f"prefill group {hq // hkv} shared {shared}")
+    check_status_clean("prefill group sweep")
+
+
 def test_prefill_late_dominant_keys_rebase():
     """Keys far into the cached prefix whose scores exceed everything before them by far more
     than the lazy re-basing threshold (2^8): rows re-base in stages wholly below the diagonal,
