@@ -179,7 +179,10 @@ int pa_combine(const float *ws_o, const float *ws_lse, int32_t batch, int32_t nu
  * is computed.)
  *   q, out         [cu_q_lens[batch], num_heads, head_dim] bf16
  *   cu_q_lens      [batch + 1] int32, non-decreasing, cu_q_lens[0] = 0
- *   max_chunk      an upper bound of max_b C_b (sizes the grid; rows beyond C_b are idle)
+ *   max_chunk      an upper bound of max_b C_b (sizes the grid; rows beyond C_b are idle).  A
+ *                  chunk longer than the grid covers is reported (PA_DEV_OUT_OF_RANGE in the
+ *                  device status) and its rows past the grid are not written; the other
+ *                  sequences' results are unaffected
  * A sequence with C_b > seq_lens[b] or seq_lens[b] > max_blocks*16 is skipped and sets
  * PA_DEV_OUT_OF_RANGE.
  */

@@ -71,6 +71,9 @@ __global__ void __launch_bounds__(kThreads) prefill_mma_kernel(const __grid_cons
     }
     const int rows = C * g;
     const int row0 = mt * kRows;
+    // a chunk longer than max_chunk would leave rows past the grid unwritten: reported
+    if (mt == 0 && kvh == 0 && threadIdx.x == 0 && (long long)(rows + kRows - 1) / kRows > gridDim.x)
+        atomicOr(a.status, kDevOutOfRange);
     if (row0 >= rows) return;  // this sequence's chunk is shorter than the grid allows
     const int last_row = min(rows, row0 + kRows) - 1;
     const int kmax = L - C + last_row / g + 1;  // keys the tile's last query sees

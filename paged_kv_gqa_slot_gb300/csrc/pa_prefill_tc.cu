@@ -182,6 +182,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         return;
     }
     const int T = (C + tpt - 1) / tpt;  // query tiles of this sequence
+    // a chunk longer than max_chunk needs more tile pairs than the grid has: its middle tiles
+    // would go unwritten, so it is reported
+    if (p == 0 && kvh == 0 && threadIdx.x == 0 && (T + 1) / 2 > (int)gridDim.x) atomicOr(a.status, kDevOutOfRange);
     int mtile[kTiles], ntiles[kTiles];
     pair_tiles(p, T, mtile[0], mtile[1]);
 #pragma unroll

@@ -95,6 +95,7 @@ struct Tc2Args {
     __nv_bfloat16* out;
     unsigned* status;
     int max_blocks, num_heads, num_kv_heads, num_blocks, group;
+    int q_rows;        // tokens the q map covers (batch * max_chunk)
     float scale_log2;  // scale * log2(e), signed
 };
 
@@ -202,6 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         return;
     }
     const int T = (C + tpt - 1) / tpt;  // query tiles of this sequence
+    // a chunk longer than max_chunk needs more tile pairs than the grid has: its middle tiles
+    // would go unwritten, so it is reported
+    if (p == 0 && kvh == 0 && threadIdx.x == 0 && (T + 1) / 2 > (int)gridDim.x) atomicOr(a.status, kDevOutOfRange);
     int mtile[kTiles], nst[kTiles];
     pair_tiles(p, T, mtile[0], mtile[1]);
 #pragma unroll
@@ -382,7 +386,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         // A negative scale enters as -Q (exact in bf16) against |scale|, so the row maximum is
         // always taken over the scores as they are; such Q is negated on the way in, by threads.
         const bool neg = a.scale_log2 < 0.f;
-        const bool whole = ntok == tpt && !neg;     // a whole tile at a positive scale: Q by TMA
+        // a whole tile at a positive scale inside the rows the q map covers: Q by TMA (a chunk
+        // longer than max_chunk can put a later sequence's tiles past them)
+        const bool whole = ntok == tpt && !neg && q0 + tok0 + tpt <= a.q_rows;
         const bool valid = r < ntok * g;
         const int qi = r / g, h = r % g;
         const int pos = valid ? L - C + tok0 + qi : -1;  // causal limit of the row (inclusive)
@@ -577,6 +583,7 @@ cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStre
     t.num_kv_heads = pool.num_kv_heads;
     t.num_blocks = pool.num_blocks;
     t.group = g;
+    t.q_rows = (int)std::min<long long>(tokens, 0x7fffffffLL);
     t.scale_log2 = a.scale * kLog2e;
     const int tiles = std::max(1, (a.max_chunk + tpt - 1) / tpt);
     const int pairs = (tiles + 1) / 2;

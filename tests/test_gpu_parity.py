@@ -568,6 +568,19 @@ def test_decode_seq_len_past_table_is_flagged():
     compare(out[[0, 2]], ref[[0, 2]], "decode beside a clamped sequence")
 
 
+def test_prefill_max_chunk_below_a_chunk_is_flagged():
+    """max_chunk smaller than a sequence's chunk: that chunk's tiles past the grid cannot be
+    computed, and the device status says so; a chunk the grid covers comes out right."""
+    case = W.paged_case(name="short_max_chunk", seed=5605, seq_lens=[400, 300], q_lens=[100, 40], new_lens=[100, 40],
+                        num_heads=32, num_kv_heads=8, head_dim=128, num_blocks=64)
+    g = GpuCase(case)
+    pa.pa_device_status(clear=True)
+    out = pa.pa_prefill_chunked(g.pool, g.q, g.cu, g.bt, g.sl, case.scale, 50)
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    ref = oracle_prefill(case)
+    compare(out[100:], ref[100:], "the chunk the grid covers, beside one it does not")
+
+
 def test_prefill_invalid_sequence_is_skipped():
     """A sequence whose chunk is longer than its length is skipped and flagged: its rows are
     not written, and the sequences around it come out right."""
@@ -668,6 +681,15 @@ cases = [
 for i, c in enumerate(cases):
     compare(GpuCase(c).prefill(), oracle_prefill(c), f"{sys.argv[2]} prefill case {i}")
     check_status_clean(f"{sys.argv[2]} prefill case {i}")
+# max_chunk below a chunk's length is reported; the chunk the grid covers is right
+import paged_kv_gqa_slot_gb300 as pa
+c = W.paged_case(name="short_max_chunk", seed=5605, seq_lens=[400, 300], q_lens=[100, 40], new_lens=[100, 40],
+                 num_heads=32, num_kv_heads=8, head_dim=128, num_blocks=64)
+g = GpuCase(c)
+pa.pa_device_status(clear=True)
+out = pa.pa_prefill_chunked(g.pool, g.q, g.cu, g.bt, g.sl, c.scale, 50)
+assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE, "short max_chunk not reported"
+compare(out[100:], oracle_prefill(c)[100:], f"{sys.argv[2]} chunk the grid covers")
 print("ok")
 '''
 
