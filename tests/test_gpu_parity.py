@@ -581,6 +581,23 @@ def test_prefill_max_chunk_below_a_chunk_is_flagged():
     compare(out[100:], ref[100:], "the chunk the grid covers, beside one it does not")
 
 
+def test_prefill_flags_out_of_pool_block():
+    """A block id past the pool in one sequence's table is reported, read as a valid block
+    instead (never out of bounds), and leaves the other sequences' results right."""
+    case = W.random_case(5606, batch=3, num_heads=32, num_kv_heads=8, head_dim=128, min_len=150, max_len=300,
+                         q_len=80, prefill=True)
+    g = GpuCase(case)
+    bt = case.block_tables.clone()
+    bt[1, 2] = case.num_blocks + 5
+    pa.pa_device_status(clear=True)
+    out = pa.pa_prefill_chunked(g.pool, g.q, g.cu, bt.cuda(), g.sl, case.scale, max(case.q_lens))
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    ref = oracle_prefill(case)
+    cu = case.cu_q_lens.tolist()
+    keep = np.r_[cu[0]:cu[1], cu[2]:cu[3]]
+    compare(out[torch.from_numpy(keep).to(out.device)], ref[keep], "prefill beside a sequence with a bad block id")
+
+
 def test_prefill_invalid_sequence_is_skipped():
     """A sequence whose chunk is longer than its length is skipped and flagged: its rows are
     not written, and the sequences around it come out right."""
@@ -690,6 +707,19 @@ pa.pa_device_status(clear=True)
 out = pa.pa_prefill_chunked(g.pool, g.q, g.cu, g.bt, g.sl, c.scale, 50)
 assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE, "short max_chunk not reported"
 compare(out[100:], oracle_prefill(c)[100:], f"{sys.argv[2]} chunk the grid covers")
+# a block id past the pool is reported; the other sequences are right
+import numpy as np
+c = W.random_case(5606, batch=3, num_heads=32, num_kv_heads=8, head_dim=128, min_len=150, max_len=300, q_len=80,
+                  prefill=True)
+g = GpuCase(c)
+bt = c.block_tables.clone()
+bt[1, 2] = c.num_blocks + 5
+pa.pa_device_status(clear=True)
+out = pa.pa_prefill_chunked(g.pool, g.q, g.cu, bt.cuda(), g.sl, c.scale, max(c.q_lens))
+assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE, "bad block id not reported"
+cu = c.cu_q_lens.tolist()
+keep = np.r_[cu[0]:cu[1], cu[2]:cu[3]]
+compare(out[torch.from_numpy(keep).to(out.device)], oracle_prefill(c)[keep], f"{sys.argv[2]} beside a bad block id")
 print("ok")
 '''
 
