@@ -579,6 +579,15 @@ def test_prefill_max_chunk_below_a_chunk_is_flagged():
     assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
     ref = oracle_prefill(case)
     compare(out[100:], ref[100:], "the chunk the grid covers, beside one it does not")
+    # the same on the multi-query decode route (max_chunk x g <= 16): a 10-query chunk against
+    # max_chunk 4 is reported and skipped, the 3-query chunk beside it is right
+    case = W.paged_case(name="short_max_chunk_mq", seed=5607, seq_lens=[300, 200], q_lens=[10, 3], new_lens=[10, 3],
+                        num_heads=32, num_kv_heads=8, head_dim=128, num_blocks=48)
+    g = GpuCase(case)
+    pa.pa_device_status(clear=True)
+    out = pa.pa_prefill_chunked(g.pool, g.q, g.cu, g.bt, g.sl, case.scale, 4)
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_OUT_OF_RANGE
+    compare(out[10:], oracle_prefill(case)[10:], "a short chunk on the multi-query route beside an over-long one")
 
 
 def test_prefill_flags_out_of_pool_block():
