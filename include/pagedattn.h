@@ -199,6 +199,16 @@ int pa_prefill_chunked(const pa_pool *pool, const void *q, const int32_t *cu_q_l
 int pa_device_status(uint32_t *flags, int32_t clear, pa_stream_t stream);
 
 /*
+ * pa_selftest_wait_timeout -- a check of the error path the device status describes: one
+ * thread waits, through the same bounded-wait helper the kernels use, on an mbarrier that
+ * nothing ever arrives on, gives up after `limit_cycles` SM cycles (1 .. 2^40) and sets
+ * PA_DEV_TIMEOUT, so that pa_device_status afterwards returns PA_ERR_TIMEOUT.  Nothing faults
+ * and the context stays usable.  Asynchronous on `stream`.  Returns PA_OK,
+ * PA_ERR_INVALID_ARG for a limit outside the range, or PA_ERR_CUDA.
+ */
+int pa_selftest_wait_timeout(uint64_t limit_cycles, pa_stream_t stream);
+
+/*
  * pa_decode_splitkv_noalloc -- split-KV decode and its log-sum-exp merge in one call that
  * allocates nothing and takes no workspace: out = pa_combine(pa_decode_splitkv(...)).
  * The pages have no counterpart of this call; it exists for callers that cannot allocate

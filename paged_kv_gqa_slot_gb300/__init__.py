@@ -22,7 +22,7 @@ import torch
 
 __all__ = ["PaPool", "pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decode", "pa_decode_splitkv",
            "pa_combine", "pa_prefill_chunked",
-           "pa_device_status", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "pa_splitkv_num_partitions",
+           "pa_device_status", "pa_selftest_wait_timeout", "pa_splitkv_workspace_bytes", "pa_decode_num_splits", "pa_splitkv_num_partitions",
            "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes", "PagedAttnError",
            "BlockManager", "pa_kv_block_bytes", "pa_kv_budget_blocks",
            "library", "library_path", "BLOCK_SIZE", "EXPORTED_SYMBOLS"]
@@ -34,6 +34,7 @@ EXPORTED_SYMBOLS = ("pa_kv_append", "pa_kv_copy", "pa_decode", "pa_append_decode
                     "pa_decode_splitkv", "pa_combine",
                     "pa_prefill_chunked", "pa_device_status", "pa_decode_num_splits", "pa_splitkv_num_partitions",
                     "pa_status_str", "pa_version", "pa_decode_splitkv_noalloc", "pa_noalloc_scratch_bytes",
+                    "pa_selftest_wait_timeout",
                     "pa_kv_block_bytes", "pa_kv_budget_blocks", "pa_bm_create", "pa_bm_destroy", "pa_bm_admit", "pa_bm_admit_cow",
                     "pa_bm_commit", "pa_bm_release", "pa_bm_slots", "pa_bm_stats")
 
@@ -88,6 +89,7 @@ def library() -> ctypes.CDLL:
         "pa_combine": (ctypes.c_int, [P, P, I32, I32, I32, I32, P, P]),
         "pa_prefill_chunked": (ctypes.c_int, [pool, P, P, P, I32, P, I32, I32, I32, F32, P, P]),
         "pa_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32), I32, P]),
+        "pa_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, P]),
         "pa_decode_num_splits": (ctypes.c_int, [I32, I32, I32]),
         "pa_splitkv_num_partitions": (ctypes.c_int, [I32, I32, I32]),
         "pa_decode_splitkv_noalloc": (ctypes.c_int, [pool, P, P, I32, P, I32, I32, F32, I32, P, P]),
@@ -318,6 +320,12 @@ def pa_device_status(clear: bool = True, stream=None) -> int:
     if rc == PA_ERR_CUDA:
         raise PagedAttnError("pa_device_status", rc)
     return int(flags.value)
+
+
+def pa_selftest_wait_timeout(limit_cycles: int = 2_000_000, stream=None) -> None:
+    """Make one bounded device wait run out (an mbarrier nothing arrives on); afterwards the
+    device status has PA_DEV_TIMEOUT set.  Asynchronous on `stream`."""
+    _check(library().pa_selftest_wait_timeout(int(limit_cycles), _stream(stream)), "pa_selftest_wait_timeout")
 
 
 def pa_decode_num_splits(batch: int, num_kv_heads: int, max_blocks: int) -> int:

@@ -396,6 +396,13 @@ int pa_device_status(uint32_t* flags, int32_t clear, pa_stream_t stream) {
     return PA_OK;
 }
 
+int pa_selftest_wait_timeout(uint64_t limit_cycles, pa_stream_t stream) {
+    if (limit_cycles < 1 || limit_cycles > (1ull << 40)) return PA_ERR_INVALID_ARG;
+    unsigned* p = device_status_ptr();
+    if (!p) return PA_ERR_CUDA;
+    return from_cuda(launch_selftest_wait(p, (long long)limit_cycles, (cudaStream_t)stream));
+}
+
 int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks) {
     if (batch <= 0 || num_kv_heads <= 0 || max_blocks <= 0) return 1;
     return decode_splits_for(batch, num_kv_heads, max_blocks);

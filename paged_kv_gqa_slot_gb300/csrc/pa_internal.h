@@ -107,6 +107,7 @@ inline cudaLaunchAttribute pdl_attribute() {
 
 cudaError_t launch_kv_append(const PoolView& pool, const void* k_new, const void* v_new, const int64_t* slots,
                              int num_tokens, unsigned* status, cudaStream_t stream);
+cudaError_t launch_selftest_wait(unsigned* status, long long limit_cycles, cudaStream_t stream);
 cudaError_t launch_kv_copy(const PoolView& pool, const int64_t* src_slots, const int64_t* dst_slots, int n,
                            unsigned* status, cudaStream_t stream);
 cudaError_t launch_decode(const PoolView& pool, const AttnArgs& a, cudaStream_t stream);

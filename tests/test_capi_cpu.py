@@ -111,3 +111,9 @@ def test_validation_rejects_before_launch(lib):
         pa.PA_ERR_UNSUPPORTED
     # status needs a flags pointer
     assert lib.pa_device_status(None, 1, None) == pa.PA_ERR_INVALID_ARG
+
+
+def test_selftest_wait_timeout_rejects_limits_outside_its_range(lib):
+    # checked before any CUDA call, so it runs without a GPU
+    assert lib.pa_selftest_wait_timeout(0, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.pa_selftest_wait_timeout((1 << 40) + 1, None) == pa.PA_ERR_INVALID_ARG

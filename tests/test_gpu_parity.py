@@ -607,6 +607,21 @@ def test_prefill_flags_out_of_pool_block():
     compare(out[torch.from_numpy(keep).to(out.device)], ref[keep], "prefill beside a sequence with a bad block id")
 
 
+def test_bounded_wait_reports_timeout_and_context_stays_usable():
+    """A device wait that runs out (an mbarrier nothing arrives on, waited for through the
+    kernels' own bounded helper with a short limit) sets PA_DEV_TIMEOUT and returns; nothing
+    faults, and the next calls on the same context are right and report clean."""
+    import time
+    pa.pa_device_status(clear=True)
+    t0 = time.time()
+    pa.pa_selftest_wait_timeout(2_000_000)  # about a millisecond of SM cycles
+    assert pa.pa_device_status(clear=True) == pa.PA_DEV_TIMEOUT
+    assert time.time() - t0 < 5.0
+    case = W.random_case(5608, batch=4, num_heads=32, num_kv_heads=8, head_dim=128, min_len=50, max_len=400)
+    compare(GpuCase(case).decode(), oracle_decode(case), "decode right after a wait that ran out")
+    check_status_clean("after the timeout self-test")
+
+
 def test_prefill_invalid_sequence_is_skipped():
     """A sequence whose chunk is longer than its length is skipped and flagged: its rows are
     not written, and the sequences around it come out right."""
