@@ -24,8 +24,10 @@
 // holds up the other's MMAs; the two tiles' softmax warpgroups run side by side.
 // The running max is re-based lazily: O is rescaled in TMEM only when a row's max grows by
 // more than 2^8, which keeps every P <= 256 and makes rescales rare.
-// Q tiles come in by TMA through a 3-D map of q (d, head, token) whose box is one tile (a tile
-// cut short by the end of its chunk row by row instead); each row of O is stored by its thread.
+// Q tiles come in by TMA through a 3-D map of q (d, head, token) whose box is one tile; a tile
+// cut short by the end of its chunk, one at a negative scale, or one past the rows the map
+// covers is copied in row by row by its softmax threads instead.  Each row of O is stored by
+// its thread.
 // Warp roles: 0-3 softmax of tile 0, 4-7 softmax of tile 1 (TMEM lanes 32(w%4)..+31),
 // 8 MMA issue of tile 0 + TMEM owner, 9 TMA loads of K, 10 TMA loads of V, 11 MMA issue of
 // tile 1; this control warpgroup hands registers to the softmax warpgroups.  Every CTA loads its
@@ -167,6 +169,15 @@ __device__ __forceinline__ void stage_exps(const uint32_t (&s0)[32], const uint3
         }
         pw[c / 2] = pack_bf16x2(fast_exp2(x0), fast_exp2(x1));
     }
+}
+
+// (a0, a1) += the two bf16 values of a packed word, each widened exactly: the mixed-precision
+// add of sm_100 and later, in place of unpacking both halves into fp32 first.
+__device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "r"(w));
 }
 
 // O (the row's 128 fp32 columns of tensor memory at `taddr`) *= f, in 8-column pieces.
@@ -480,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int w = 0; w < kKeys / 2; w += 2) {
-                add_x2(ls[0], ls[1], bf16_lo(pw[w]), bf16_hi(pw[w]));
-                add_x2(ls[2], ls[3], bf16_lo(pw[w + 1]), bf16_hi(pw[w + 1]));
+                add_bf16x2(ls[0], ls[1], pw[w]);
+                add_bf16x2(ls[2], ls[3], pw[w + 1]);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 #pragma unroll
