@@ -7,32 +7,32 @@
 // attends causally to keys 0 .. L_s - C_s + i through the block table.
 //
 // Rows of a query tile are (query, head-of-the-group) pairs: row r = query r / g, head r % g,
-// so one K/V tile serves all g heads; a tile holds 128 rows (128 / g queries).  One CTA per
-// SM holds TWO query tiles of the same (sequence, kv head), the i-th longest with the i-th
-// shortest, so every CTA has about the same causal work.  Per stage of 64 keys (four
-// 16-token pool blocks, loaded by TMA with 128-byte swizzling), for each tile t:
-//   S_t[128 x 64] = Q_t K^T     tcgen05.mma, M=128 N=64, Q_t (A) and K (B) from smem
+// so one K/V tile serves all g heads; a tile holds 128 rows (128 / g queries).  One CTA holds
+// ONE query tile, and two CTAs are resident on every SM (256 TMEM columns and 112 KB of shared
+// memory each): the two run independently, so one's start-up and epilogue overlap the other's
+// stages, and the hardware scheduler hands the next tile to whichever SM slot frees first.
+// Tiles launch longest first (the last tile of every chunk, then the one before it, ...), so
+// the short tiles fill in behind the long ones.  Per stage of 64 keys (four 16-token pool
+// blocks, loaded by TMA with 128-byte swizzling):
+//   S[128 x 64] = Q K^T       tcgen05.mma, M=128 N=64, Q (A) and K (B) from smem
 //   softmax          one thread per row reads its S row from TMEM, masks causally (only in
 //                    stages that cross the diagonal), keeps an online max / sum in base 2 and
-//                    writes P (bf16, two keys per column) over the first 32 columns of S_t
-//   O_t += P_t V     tcgen05.mma, M=128 N=128, P_t (A) from TMEM, V (B) from smem
-// Tensor memory: tile t owns columns [256t, 256t+256): two 64-column score buffers, stage j
-// in buffer j % 2, and O_t [128, 256).  So S_t(j+1) is computed while the softmax works on
-// stage j, and P_t V(j) only gates S_t(j+2), which reuses the buffer P_t(j) sits in: the
-// tensor core runs one issuer's MMAs in order, and tile t's MMA warp issues, per stage j,
-// P_t V(j) then S_t(j+2).  Each tile has its own MMA warp, so a tile waiting for its P never
-// holds up the other's MMAs; the two tiles' softmax warpgroups run side by side.
+//                    writes P (bf16, two keys per column) over the first 32 columns of S
+//   O += P V         tcgen05.mma, M=128 N=128, P (A) from TMEM, V (B) from smem
+// Tensor memory: two 64-column score buffers, stage j in buffer j % 2, and O at [128, 256).
+// So S(j+1) is computed while the softmax works on stage j, and P V(j) only gates S(j+2),
+// which reuses the buffer P(j) sits in: the tensor core runs one issuer's MMAs in order, and
+// the MMA warp issues, per stage j, P V(j) then S(j+2).
 // The running max is re-based lazily: O is rescaled in TMEM only when a row's max grows by
 // more than 2^8, which keeps every P <= 256 and makes rescales rare.
 // Q tiles come in by TMA through a 3-D map of q (d, head, token) whose box is one tile; a tile
 // cut short by the end of its chunk, one at a negative scale, or one past the rows the map
 // covers is copied in row by row by its softmax threads instead.  Each row of O is stored by
 // its thread.
-// Warp roles: 0-3 softmax of tile 0, 4-7 softmax of tile 1 (TMEM lanes 32(w%4)..+31),
-// 8 MMA issue of tile 0 + TMEM owner, 9 TMA loads of K, 10 TMA loads of V, 11 MMA issue of
-// tile 1; this control warpgroup hands registers to the softmax warpgroups.  Every CTA loads its
-// own K/V; the CTAs of one (sequence, kv head) -- and, with a shared prefix, of every
-// sequence that shares it -- read the same pool blocks, the copies after the first from L2.
+// Warp roles: 0-3 softmax (TMEM lanes 32w..32w+31), 4 MMA issue + TMEM owner, 5 TMA loads of
+// K, 6 TMA loads of V.  Every CTA loads its own K/V; the CTAs of one (sequence, kv head) --
+// and, with a shared prefix, of every sequence that shares it -- read the same pool blocks,
+// the copies after the first from L2.
 #include <algorithm>
 #include <cmath>
 #include <cstdlib>
@@ -44,50 +44,41 @@ namespace pa {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kRows = 128;                      // MMA M: rows of one query tile
-constexpr int kTiles = 2;                       // query tiles per CTA
+constexpr int kRows = 128;                      // MMA M: rows of the query tile
 constexpr int kKeys = 64;                       // keys per stage (MMA N of S, K of P V)
-constexpr int kKStages = 4, kVStages = 4;       // K and V ring slots
-constexpr int kSoftmaxThreads = kTiles * 128;
-// control warpgroup: MMA issue for tile 0 (and TMEM owner), TMA loads of K, of V, MMA issue for tile 1
-constexpr int kMmaWarp = kSoftmaxThreads / 32, kKLoadWarp = kMmaWarp + 1, kVLoadWarp = kMmaWarp + 2,
-              kMmaWarp1 = kMmaWarp + 3;
-constexpr int kThreads = kSoftmaxThreads + 128;
-static_assert(kMmaWarp1 == kThreads / 32 - 1, "warp roles");
-// Registers: launched at kLaunchRegs a thread (65536 / 384 threads), the control warpgroup
-// gives some back and the softmax warpgroups take them (setmaxnreg); the shares add up to
-// exactly the launch's total, and the launcher checks the compiled count.
-constexpr int kLaunchRegs = 168, kSoftmaxRegs = 208, kControlRegs = 88;
-static_assert(kSoftmaxThreads * kSoftmaxRegs + 128 * kControlRegs == kThreads * kLaunchRegs, "register split");
-constexpr int kTmemCols = 512;
-constexpr uint32_t kTmemTile = 256;             // columns owned by one tile
+constexpr int kKStages = 3, kVStages = 2;       // K and V ring slots (a third K slot measured 1% faster)
+constexpr int kSoftmaxThreads = 128;
+constexpr int kMmaWarp = kSoftmaxThreads / 32, kKLoadWarp = kMmaWarp + 1, kVLoadWarp = kMmaWarp + 2;
+constexpr int kThreads = kSoftmaxThreads + 96;
+constexpr int kCtasPerSm = 2;                   // resident CTAs an SM holds (tensor memory, shared memory)
+constexpr int kTmemCols = 256;                  // half of an SM's tensor memory
 constexpr uint32_t kTmemS = 0, kTmemO = 128;    // score buffers at 0 and 64, O at 128
 constexpr int kQHalf = kRows * 128;             // [128 rows][64 columns] bf16 = 16 KB
-constexpr int kQTile = 2 * kQHalf;              // a Q tile: two column halves
+constexpr int kQTile = 2 * kQHalf;              // the Q tile: two column halves
 constexpr int kKVHalf = kKeys * 128;            // [64 keys][64 columns] bf16 = 8 KB
 constexpr int kKVStage = 2 * kKVHalf;           // one K or V stage: two column halves
 constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTiles * kQTile;
+constexpr int kOffK = kOffQ + kQTile;
 constexpr int kOffV = kOffK + kKStages * kKVStage;
 constexpr int kBarOff = kOffV + kVStages * kKVStage;
-constexpr int kSmemBytes = kBarOff + 512 + 1024;
+// The dynamic shared memory starts 1024-byte aligned (the swizzled tiles need it; the kernel
+// checks), so no slack is added: two CTAs must fit an SM's 228 KB with 1 KB reserved each.
+constexpr int kSmemBytes = kBarOff + 256;
 constexpr float kRescaleThreshold = 8.f;        // log2 units
 constexpr float kLog2e = 1.44269504088896340736f;
 
 struct Bars {
-    // a ring slot is refilled once each tile that reads it has released it (the tiles' MMAs
-    // are issued by different warps, so each commits its own release)
-    uint64_t k_full[kKStages], k_empty[kTiles][kKStages], v_full[kVStages], v_empty[kTiles][kVStages];
-    // per tile: scores and P of stage j use buffer j % 2 (a softmax may finish two stages before
-    // the MMA warp waits for the first, so one barrier per buffer keeps their phases apart);
-    // o_done completes after every P V, o_final after the tile's last one
-    uint64_t q_full[kTiles], s_full[kTiles][2], p_full[kTiles][2], o_done[kTiles], o_final[kTiles];
-    uint64_t drain[kTiles];
-    uint64_t v_zero;  // tile 0's softmax has zeroed the V rows past the sequence end
+    uint64_t k_full[kKStages], k_empty[kKStages], v_full[kVStages], v_empty[kVStages];
+    // scores and P of stage j use buffer j % 2 (the softmax may finish two stages before the
+    // MMA warp waits for the first, so one barrier per buffer keeps their phases apart);
+    // o_done completes after every P V, o_final after the last one
+    uint64_t q_full, s_full[2], p_full[2], o_done, o_final;
+    uint64_t drain;
     uint32_t tmem_base;
 };
-static_assert(sizeof(Bars) <= 512, "barrier block");
-static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(kCtasPerSm * (kSmemBytes + 1024) <= 228 * 1024, "shared memory for two resident CTAs");
+static_assert(kCtasPerSm * kTmemCols <= 512, "tensor memory for two resident CTAs");
 
 struct Tc2Args {
     const __nv_bfloat16* q;
@@ -96,7 +87,8 @@ struct Tc2Args {
     const int32_t* cu_q_lens;
     __nv_bfloat16* out;
     unsigned* status;
-    int max_blocks, num_heads, num_kv_heads, num_blocks, group;
+    int max_blocks, num_heads, num_kv_heads, num_blocks, group, batch;
+    int tiles;         // tile ranks the grid holds per (sequence, kv head)
     int q_rows;        // tokens the q map covers (batch * max_chunk)
     float scale_log2;  // scale * log2(e), signed
 };
@@ -106,16 +98,6 @@ __device__ __forceinline__ int tile_key_count(int mt, int tpt, int C, int L) {
     const int tok0 = mt * tpt;
     if (mt < 0 || tok0 >= C) return 0;
     return L - C + tok0 + min(tpt, C - tok0);
-}
-
-// The two query tiles of pair p out of T: the (p+1)-th longest and the (p+1)-th shortest
-// (-1: none).  Pairs p >= ceil(T / 2) hold nothing.
-__device__ __forceinline__ void pair_tiles(int p, int T, int& t0, int& t1) {
-    t0 = -1;
-    t1 = -1;
-    if (p < 0 || 2 * p >= T) return;
-    t0 = T - 1 - p;
-    t1 = p < t0 ? p : -1;
 }
 
 // bar.red.and over the `count` threads of named barrier `id`: true iff every one has `pred`.
@@ -194,57 +176,59 @@ __device__ __forceinline__ void scale_o(uint32_t taddr, float f) {
     tmem_wait_st();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                                  const __grid_constant__ CUtensorMap tm_v,
-                                                                  const __grid_constant__ CUtensorMap tm_q,
-                                                                  const __grid_constant__ Tc2Args a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                           const __grid_constant__ CUtensorMap tm_v,
+                                                                           const __grid_constant__ CUtensorMap tm_q,
+                                                                           const __grid_constant__ Tc2Args a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
     Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int p = blockIdx.x;  // tile pair
-    const int kvh = blockIdx.y, b = blockIdx.z;
+    // blockIdx.x = (rank * batch + b) * num_kv_heads + kvh, so the CTAs launch rank by rank:
+    // rank 0 is every chunk's last (longest) tile, rank 1 the one before, ...
+    const int kvh = (int)(blockIdx.x % (unsigned)a.num_kv_heads);
+    const int rb = (int)(blockIdx.x / (unsigned)a.num_kv_heads);
+    const int b = rb % a.batch, rank = rb / a.batch;
     pdl_wait();
+    if (smem_u32(smem) & 1023u) {  // the swizzled layouts need the declared alignment
+        if (threadIdx.x == 0) atomicOr(a.status, kDevOutOfRange);
+        return;
+    }
     const int g = a.group, tpt = kRows / g;
     const int q0 = a.cu_q_lens[b];
     const int C = a.cu_q_lens[b + 1] - q0;
     const int L = a.seq_lens[b];
     if (C < 0 || L < C || L > a.max_blocks * kBlockSize) {
-        if (threadIdx.x == 0 && p == 0 && kvh == 0) atomicOr(a.status, kDevOutOfRange);
+        if (threadIdx.x == 0 && rank == 0 && kvh == 0) atomicOr(a.status, kDevOutOfRange);
         return;
     }
     const int T = (C + tpt - 1) / tpt;  // query tiles of this sequence
-    // a chunk longer than max_chunk needs more tile pairs than the grid has: its middle tiles
-    // would go unwritten, so it is reported
-    if (p == 0 && kvh == 0 && threadIdx.x == 0 && (T + 1) / 2 > (int)gridDim.x) atomicOr(a.status, kDevOutOfRange);
-    int mtile[kTiles], nst[kTiles];
-    pair_tiles(p, T, mtile[0], mtile[1]);
-#pragma unroll
-    for (int t = 0; t < kTiles; ++t) nst[t] = (tile_key_count(mtile[t], tpt, C, L) + kKeys - 1) / kKeys;
-    const int nstage = nst[0];  // tile 0 is the later one: it needs the most keys
-    if (nstage == 0) return;    // this pair holds no query of the chunk (the same for the whole CTA)
-    const int nblk = (tile_key_count(mtile[0], tpt, C, L) + kBlockSize - 1) / kBlockSize;  // pool blocks read
+    // a chunk longer than max_chunk has more tiles than the grid: the grid covers its first
+    // a.tiles tiles, and the rest is reported
+    if (rank == 0 && kvh == 0 && threadIdx.x == 0 && T > a.tiles) atomicOr(a.status, kDevOutOfRange);
+    const int covered = min(T, a.tiles);
+    if (rank >= covered) return;  // the same for the whole CTA
+    const int mt = covered - 1 - rank;
+    const int nkeys = tile_key_count(mt, tpt, C, L);
+    const int nst = (nkeys + kKeys - 1) / kKeys;               // key stages
+    const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;  // pool blocks read
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
-            for (int t = 0; t < kTiles; ++t) mbar_init(&bars->k_empty[t][s], 1);
+            mbar_init(&bars->k_empty[s], 1);
         }
         for (int s = 0; s < kVStages; ++s) {
             mbar_init(&bars->v_full[s], 1);
-            for (int t = 0; t < kTiles; ++t) mbar_init(&bars->v_empty[t][s], 1);
+            mbar_init(&bars->v_empty[s], 1);
         }
-        for (int t = 0; t < kTiles; ++t) {
-            mbar_init(&bars->q_full[t], 1);
-            mbar_init(&bars->s_full[t][0], 1);
-            mbar_init(&bars->s_full[t][1], 1);
-            mbar_init(&bars->p_full[t][0], 128);
-            mbar_init(&bars->p_full[t][1], 128);
-            mbar_init(&bars->o_done[t], 1);
-            mbar_init(&bars->o_final[t], 1);
-            mbar_init(&bars->drain[t], 1);
-        }
-        mbar_init(&bars->v_zero, 128);
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->s_full[0], 1);
+        mbar_init(&bars->s_full[1], 1);
+        mbar_init(&bars->p_full[0], 128);
+        mbar_init(&bars->p_full[1], 128);
+        mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->o_final, 1);
+        mbar_init(&bars->drain, 1);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -257,17 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
     const uint32_t tmem = bars->tmem_base;
 
     if (warp >= kMmaWarp) {
-        // control warpgroup: every warp gives registers back at this one point, then takes its role
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
         if (warp == kKLoadWarp || warp == kVLoadWarp) {
             // -------------------------------------------------------- TMA producers (K, V)
             // The 8 boxes of a stage (4 blocks x 2 column halves, 2 KB each) go out from lanes
-            // 0-7, one each; a block past the keys the pair needs reads past the pool (zeros).
+            // 0-7, one each; a block past the keys the tile needs reads past the pool (zeros).
             const bool is_k = warp == kKLoadWarp;
             const CUtensorMap* map = is_k ? &tm_k : &tm_v;
             uint64_t* full = is_k ? bars->k_full : bars->v_full;
-            uint64_t* empty0 = is_k ? bars->k_empty[0] : bars->v_empty[0];
-            uint64_t* empty1 = is_k ? bars->k_empty[1] : bars->v_empty[1];
+            uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
             uint8_t* ring = smem + (is_k ? kOffK : kOffV);
             const int nslots = is_k ? kKStages : kVStages;
             if (lane == 0) prefetch_tensormap(map);
@@ -280,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
             const int box_t = lane >> 1, box_h = lane & 1;
             bool ok = true;
             int issued = 0;
-            for (int j = 0; j < nstage && ok; ++j) {
+            for (int j = 0; j < nst && ok; ++j) {
                 if (4 * j >= c0 + 32) {
                     c0 += 32;
                     cur = nxt;
@@ -293,13 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                 const int row = lb < nblk ? (id * a.num_kv_heads + kvh) * kBlockSize : oob_row;
                 const int s = j % nslots;
                 if (lane == 0) {
-                    // the slot's previous stage, j - nslots, was read by tile 0 and, if it is one
-                    // of its stages, by tile 1
-                    if (j >= nslots) {
-                        const uint32_t par = ((j / nslots) & 1) ^ 1;
-                        ok = mbar_wait(&empty0[s], par);
-                        if (ok && j - nslots < nst[1]) ok = mbar_wait(&empty1[s], par);
-                    }
+                    // the slot's previous stage, j - nslots, has been read
+                    if (j >= nslots) ok = mbar_wait(&empty[s], ((j / nslots) & 1) ^ 1);
                     if (ok) mbar_arrive_expect_tx(&full[s], kKVStage);
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
@@ -317,48 +293,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                 if (!ok) atomicOr(a.status, kDevTimeout);
             }
         } else {
-            // -------------------------------------------------------- MMA issue, one warp per tile
-            // Each tile's chain -- its P(j), then P V(j), then S(j+2) into the buffer P(j) held --
-            // runs in its own warp, so while one warp waits for its tile's P the other keeps the
-            // tensor core busy (a waiting issuer leaves it idle: issue runs only a few MMAs
-            // ahead of execution).  The warp runs the loop together and one elected lane issues,
-            // so every operand is warp-uniform; waits give one verdict for the warp.  Operand
+            // -------------------------------------------------------- MMA issue
+            // The tile's chain -- P(j), then P V(j), then S(j+2) into the buffer P(j) held -- in
+            // one warp; the other resident CTA's MMA warp keeps the tensor core busy while this
+            // one waits (a waiting issuer leaves it idle: issue runs only a few MMAs ahead of
+            // execution).  The warp runs the loop together and one elected lane issues, so
+            // every operand is warp-uniform; waits give one verdict for the warp.  Operand
             // descriptors are built once; a stage or a k-step only moves the start address,
             // which adds (offset >> 4) to the low field (no carry: every shared address is
             // below 2^18).
-            const int t = warp == kMmaWarp1 ? 1 : 0;
-            const int n = nst[t];
-            // the one stage whose V rows past the sequence end tile 0's softmax zeroes (-1: none)
-            const int jz = kKeys * nst[0] > L ? nst[0] - 1 : -1;
+            const int n = nst;
             constexpr uint32_t idesc_s = tc_idesc_bf16(kRows, kKeys, false);
             constexpr uint32_t idesc_o = tc_idesc_bf16(kRows, kD, true);
-            const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ + t * kQTile), 0, 1024);
+            const uint64_t qd = smem_desc_sw128(smem_u32(smem + kOffQ), 0, 1024);
             const uint64_t kdesc0 = smem_desc_sw128(smem_u32(smem + kOffK), 0, 1024);
             const uint64_t vdesc0 = smem_desc_sw128(smem_u32(smem + kOffV), kKVHalf, 1024);
-            const uint32_t tm_t = tmem + t * kTmemTile;
             auto issue_qk = [&](int j) {  // S(j) = Q K(j)^T into score buffer j % 2
                 const uint64_t kd = kdesc0 + (uint64_t)(((j % kKStages) * kKVStage) >> 4);
-                const uint32_t tm_s = tm_t + kTmemS + 64 * (j & 1);
+                const uint32_t tm_s = tmem + kTmemS + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk)
                     tc_mma_ew(tm_s, qd + (uint64_t)(((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4),
                               kd + (uint64_t)(((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4), idesc_s, kk > 0 ? 1u : 0u);
-                tc_commit_ew(&bars->s_full[t][j & 1]);
-                tc_commit_ew(&bars->k_empty[t][j % kKStages]);
+                tc_commit_ew(&bars->s_full[j & 1]);
+                tc_commit_ew(&bars->k_empty[j % kKStages]);
             };
             auto issue_pv = [&](int j) {  // O += P(j) V(j), P(j) in score buffer j % 2
                 const uint64_t vd = vdesc0 + (uint64_t)(((j % kVStages) * kKVStage) >> 4);
-                const uint32_t tm_p = tm_t + kTmemS + 64 * (j & 1);
+                const uint32_t tm_p = tmem + kTmemS + 64 * (j & 1);
 #pragma unroll
                 for (int kk = 0; kk < kKeys / 16; ++kk)
-                    tc_mma_ts_ew(tm_t + kTmemO, tm_p + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                    tc_mma_ts_ew(tmem + kTmemO, tm_p + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                  (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit_ew(&bars->o_done[t]);
-                tc_commit_ew(&bars->v_empty[t][j % kVStages]);
-                if (j + 1 == n) tc_commit_ew(&bars->o_final[t]);
+                tc_commit_ew(&bars->o_done);
+                tc_commit_ew(&bars->v_empty[j % kVStages]);
+                if (j + 1 == n) tc_commit_ew(&bars->o_final);
             };
-            bool ok = true;
-            if (n > 0) ok = mbar_wait_warp(&bars->q_full[t], 0);
+            bool ok = mbar_wait_warp(&bars->q_full, 0);
             // stages 0 and 1 into the two score buffers
             for (int j = 0; j < 2 && j < n && ok; ++j) {
                 ok = mbar_wait_warp(&bars->k_full[j], 0);
@@ -367,14 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                 issue_qk(j);
             }
             for (int j = 0; j < n && ok; ++j) {
-                // The operands the stage needs besides P -- V(j), K(j+2) and, for tile 1, the
-                // zeroed tail of V -- are waited for first (they are normally long in place),
-                // so that once P(j) is complete P V(j) and S(j+2) go out back to back.
+                // The operands the stage needs besides P -- V(j) and K(j+2) -- are waited for
+                // first (they are normally long in place), so that once P(j) is complete P V(j)
+                // and S(j+2) go out back to back.
                 ok = mbar_wait_warp(&bars->v_full[j % kVStages], (j / kVStages) & 1);
                 if (ok && j + 2 < n) ok = mbar_wait_warp(&bars->k_full[(j + 2) % kKStages], ((j + 2) / kKStages) & 1);
-                // tile 1 reads the zeroed rows only once tile 0's softmax has written them
-                if (ok && t == 1 && j == jz) ok = mbar_wait_warp(&bars->v_zero, 0);
-                if (ok) ok = mbar_wait_warp(&bars->p_full[t][j & 1], (j >> 1) & 1);
+                if (ok) ok = mbar_wait_warp(&bars->p_full[j & 1], (j >> 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(j);
@@ -382,18 +351,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                 if (j + 2 < n) issue_qk(j + 2);
             }
             // every MMA this warp issued has finished before the tensor memory is released
-            tc_commit_ew(&bars->drain[t]);
-            if (!mbar_wait_warp(&bars->drain[t], 0)) ok = false;
+            tc_commit_ew(&bars->drain);
+            if (!mbar_wait_warp(&bars->drain, 0)) ok = false;
             if (!ok && lane == 0) atomicOr(a.status, kDevTimeout);
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
         // ------------------------------------------------------------ softmax: one row per thread
-        const int t = warp >> 2;                    // query tile of this warpgroup
-        const int r = threadIdx.x & (kRows - 1);    // TMEM lane r, MMA row r
-        const int mt = t == 0 ? mtile[0] : mtile[1], nt = t == 0 ? nst[0] : nst[1];
+        const int r = threadIdx.x;                  // TMEM lane r, MMA row r
+        const int nt = nst;
         const int tok0 = mt * tpt;
-        const int ntok = (mt >= 0 && tok0 < C) ? min(tpt, C - tok0) : 0;
+        const int ntok = min(tpt, C - tok0);        // >= 1: the tile holds a query of the chunk
         // A negative scale enters as -Q (exact in bf16) against |scale|, so the row maximum is
         // always taken over the scores as they are; such Q is negated on the way in, by threads.
         const bool neg = a.scale_log2 < 0.f;
@@ -404,38 +371,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         const int qi = r / g, h = r % g;
         const int pos = valid ? L - C + tok0 + qi : -1;  // causal limit of the row (inclusive)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        const uint32_t tm_row = tmem + lane_base + t * kTmemTile;
-        uint8_t* qs = smem + kOffQ + t * kQTile;
-        const int bar_id = 1 + t;                   // named barrier of this warpgroup
-        if (nt > 0) {
-            if (whole) {
-                if (r == 0) {
-                    prefetch_tensormap(&tm_q);
-                    mbar_arrive_expect_tx(&bars->q_full[t], kQTile);
-                    tma_load_3d(qs, &tm_q, 0, kvh * g, q0 + tok0, &bars->q_full[t]);
-                    tma_load_3d(qs + kQHalf, &tm_q, 64, kvh * g, q0 + tok0, &bars->q_full[t]);
-                }
-            } else {
-                // row by row into the same 128-byte swizzled layout (zeros past the chunk); the
-                // sign bit of every bf16 flips for a negative scale
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    a.q + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD);
-                const uint32_t flip = neg ? 0x80008000u : 0u;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        uint4 v = valid ? __ldg(src + hh * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
-                        v.x ^= flip;
-                        v.y ^= flip;
-                        v.z ^= flip;
-                        v.w ^= flip;
-                        *reinterpret_cast<uint4*>(qs + hh * kQHalf + swz128(r, c)) = v;
-                    }
-                fence_proxy_async_smem();
-                named_sync(bar_id, 128);
-                if (r == 0) mbar_arrive(&bars->q_full[t]);
+        const uint32_t tm_row = tmem + lane_base;
+        uint8_t* qs = smem + kOffQ;
+        constexpr int bar_id = 1;                   // named barrier of the softmax warps
+        if (whole) {
+            if (r == 0) {
+                prefetch_tensormap(&tm_q);
+                mbar_arrive_expect_tx(&bars->q_full, kQTile);
+                tma_load_3d(qs, &tm_q, 0, kvh * g, q0 + tok0, &bars->q_full);
+                tma_load_3d(qs + kQHalf, &tm_q, 64, kvh * g, q0 + tok0, &bars->q_full);
             }
+        } else {
+            // row by row into the same 128-byte swizzled layout (zeros past the chunk); the sign
+            // bit of every bf16 flips for a negative scale
+            const uint4* src = reinterpret_cast<const uint4*>(
+                a.q + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD);
+            const uint32_t flip = neg ? 0x80008000u : 0u;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 v = valid ? __ldg(src + hh * 8 + c) : make_uint4(0u, 0u, 0u, 0u);
+                    v.x ^= flip;
+                    v.y ^= flip;
+                    v.z ^= flip;
+                    v.w ^= flip;
+                    *reinterpret_cast<uint4*>(qs + hh * kQHalf + swz128(r, c)) = v;
+                }
+            fence_proxy_async_smem();
+            named_sync(bar_id, 128);
+            if (r == 0) mbar_arrive(&bars->q_full);
         }
         const float sl = fabsf(a.scale_log2);  // Q carries the sign
         float m_used = -INFINITY, l = 0.f;
@@ -444,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
         // that gave up, a rescale of O) is taken by the whole warp.
         for (int j = 0; j < nt; ++j) {
             const uint32_t sbuf = tm_row + kTmemS + 64 * (j & 1);
-            if (__any_sync(0xffffffffu, !mbar_wait(&bars->s_full[t][j & 1], (j >> 1) & 1))) {
+            if (__any_sync(0xffffffffu, !mbar_wait(&bars->s_full[j & 1], (j >> 1) & 1))) {
                 ok = false;
                 break;
             }
@@ -465,11 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
             const float m_new = fmaxf(m_used, mxs);
             const bool rebase = m_new > m_used + kRescaleThreshold;  // always for the first visible key
             if (__any_sync(0xffffffffu, rebase && m_used != -INFINITY)) {
-                // O_t changes only once P_t V(j-1) -- which may still run, since S_t(j) was
-                // ready long before -- has finished: its commit is o_done phase j-1 (phases up
-                // to j-2 are complete, as S_t(j) was issued after P_t V(j-2), and P_t V(j) waits
-                // for this stage's P, so the parity cannot alias)
-                if (j > 0 && __any_sync(0xffffffffu, !mbar_wait(&bars->o_done[t], (j - 1) & 1))) {
+                // O changes only once P V(j-1) -- which may still run, since S(j) was ready long
+                // before -- has finished: its commit is o_done phase j-1 (phases up to j-2 are
+                // complete, as S(j) was issued after P V(j-2), and P V(j) waits for this stage's
+                // P, so the parity cannot alias)
+                if (j > 0 && __any_sync(0xffffffffu, !mbar_wait(&bars->o_done, (j - 1) & 1))) {
                     ok = false;
                     break;
                 }
@@ -500,11 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                 tmem_st8_nowait(sbuf + 8 * i, pw[8 * i], pw[8 * i + 1], pw[8 * i + 2], pw[8 * i + 3], pw[8 * i + 4],
                                 pw[8 * i + 5], pw[8 * i + 6], pw[8 * i + 7]);
             tmem_wait_st();
-            if (t == 0 && k0 + kKeys > L) {
+            if (k0 + kKeys > L) {
                 // keys at or past the sequence end: zero their V rows, whatever the slots hold
                 // (P is 0 there, but 0 times a NaN left in a slot is NaN).  Once V(j) has landed,
-                // its slot's previous readers have finished (the refill waited for them); tile
-                // 0's P V(j) follows its P(j), and tile 1's waits for the v_zero arrival below.
+                // its slot's previous reader has finished (the refill waited for it); P V(j)
+                // follows this stage's P.
                 const int s = j % kVStages;
                 if (__any_sync(0xffffffffu, !mbar_wait(&bars->v_full[s], (j / kVStages) & 1))) {
                     ok = false;
@@ -518,14 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
                     *reinterpret_cast<uint4*>(vt + half * kKVHalf + row * 128 + cc * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
-                mbar_arrive(&bars->v_zero);  // tile 1's P V of this stage waits for it
             }
             tc_fence_before();
-            mbar_arrive(&bars->p_full[t][j & 1]);
+            mbar_arrive(&bars->p_full[j & 1]);
         }
-        if (nt > 0) {
-            if (ok) ok = !__any_sync(0xffffffffu, !mbar_wait(&bars->o_final[t], 0));
-            // one verdict for the warpgroup, which then takes the same path
+        {
+            if (ok) ok = !__any_sync(0xffffffffu, !mbar_wait(&bars->o_final, 0));
+            // one verdict for the softmax warps, which then take the same path
             const bool all_ok = named_sync_all(bar_id, 128, ok);
             if (all_ok) {
                 tc_fence_after();
@@ -567,12 +531,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc2_kernel(const __grid_c
 cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
     static OncePerDevice configured;
     const cudaError_t e = configured.run([] {
-        // the register split is sound only at the launch count it was sized for
-        cudaFuncAttributes fa;
-        cudaError_t r = cudaFuncGetAttributes(&fa, prefill_tc2_kernel);
-        if (r != cudaSuccess) return r;
-        if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-        return cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        cudaError_t r = cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        // all of the SM's unified memory as shared memory, so that two CTAs fit
+        if (r == cudaSuccess)
+            r = cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     (int)cudaSharedmemCarveoutMaxShared);
+        return r;
     });
     if (e != cudaSuccess) return e;
     const int g = a.num_heads / pool.num_kv_heads;
@@ -597,9 +561,12 @@ cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStre
     t.q_rows = (int)std::min<long long>(tokens, 0x7fffffffLL);
     t.scale_log2 = a.scale * kLog2e;
     const int tiles = std::max(1, (a.max_chunk + tpt - 1) / tpt);
-    const int pairs = (tiles + 1) / 2;
+    t.batch = a.batch;
+    t.tiles = tiles;
+    const long long ctas = (long long)tiles * a.batch * pool.num_kv_heads;
+    if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;  // more CTAs than a grid holds
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pairs, pool.num_kv_heads, a.batch);
+    cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

@@ -517,8 +517,9 @@ def test_decode_large_batch_and_pool():
 
 
 def test_prefill_whole_sequence_chunks():
-    """Chunks that are the whole sequence (no cached prefix): 1000 queries (32 query tiles,
-    16 tile pairs), an odd tile count (517 queries) and a single token."""
+    """Chunks that are the whole sequence (no cached prefix): 1000 queries (32 query tiles, one
+    CTA each), an odd tile count (517 queries) and a single token, in one launch whose shorter
+    chunks leave most of the grid's tile ranks empty."""
     case = W.paged_case(name="whole_seq", seed=5601, seq_lens=[1000, 517, 1], q_lens=[1000, 517, 1],
                         new_lens=[1000, 517, 1], num_heads=32, num_kv_heads=8, head_dim=128, num_blocks=256)
     g = GpuCase(case)
