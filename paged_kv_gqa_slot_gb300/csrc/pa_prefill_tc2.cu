@@ -162,6 +162,14 @@ __device__ __forceinline__ void add_bf16x2(float& a0, float& a1, uint32_t w) {
         : "r"(w));
 }
 
+// Prefetch one box of a 3-D tensor map into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // O (the row's 128 fp32 columns of tensor memory at `taddr`) *= f, in 8-column pieces.
 __device__ __forceinline__ void scale_o(uint32_t taddr, float f) {
 #pragma unroll 1
@@ -179,6 +187,7 @@ __device__ __forceinline__ void scale_o(uint32_t taddr, float f) {
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                            const __grid_constant__ CUtensorMap tm_v,
                                                                            const __grid_constant__ CUtensorMap tm_q,
+                                                                           const __grid_constant__ CUtensorMap tm_o,
                                                                            const __grid_constant__ Tc2Args a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
@@ -211,6 +220,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
     const int nkeys = tile_key_count(mt, tpt, C, L);
     const int nst = (nkeys + kKeys - 1) / kKeys;               // key stages
     const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;  // pool blocks read
+    const int tok0 = mt * tpt;
+    const int ntok = min(tpt, C - tok0);  // >= 1: the tile holds a query of the chunk
+    // A negative scale enters as -Q (exact in bf16) against |scale|, so the row maximum is
+    // always taken over the scores as they are; such Q is negated on the way in, by threads.
+    const bool neg = a.scale_log2 < 0.f;
+    // a whole tile inside the rows the q map covers (a chunk longer than max_chunk can put a
+    // later sequence's tiles past them): Q by TMA at a positive scale
+    const bool whole = ntok == tpt && q0 + tok0 + tpt <= a.q_rows;
+
+    // The loads the first stage waits on start before the set-up below: the producers' first
+    // block-table entries, and the Q tile and the tensor maps into L2 / the map cache.
+    const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks;
+    int cur = 0, nxt = 0;
+    if (warp == kKLoadWarp || warp == kVLoadWarp) {
+        cur = lane < nblk ? __ldg(bt + lane) : 0;
+        nxt = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
+        if (lane == 0) prefetch_tensormap(warp == kKLoadWarp ? &tm_k : &tm_v);
+    } else if (threadIdx.x == 32 && whole && !neg) {
+        prefetch_tensormap(&tm_q);
+        tma_prefetch_3d(&tm_q, 0, kvh * g, q0 + tok0);
+        tma_prefetch_3d(&tm_q, 64, kvh * g, q0 + tok0);
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKStages; ++s) {
@@ -251,13 +282,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
             uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
             uint8_t* ring = smem + (is_k ? kOffK : kOffV);
             const int nslots = is_k ? kKStages : kVStages;
-            if (lane == 0) prefetch_tensormap(map);
             const uint64_t pol = l2_evict_last_policy();  // prefix blocks are shared across sequences
-            const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks;
             const int oob_row = a.num_blocks * a.num_kv_heads * kBlockSize;
             int c0 = 0;
-            int cur = lane < nblk ? __ldg(bt + lane) : 0;
-            int nxt = 32 + lane < nblk ? __ldg(bt + 32 + lane) : 0;
             const int box_t = lane >> 1, box_h = lane & 1;
             bool ok = true;
             int issued = 0;
@@ -359,14 +386,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
         // ------------------------------------------------------------ softmax: one row per thread
         const int r = threadIdx.x;                  // TMEM lane r, MMA row r
         const int nt = nst;
-        const int tok0 = mt * tpt;
-        const int ntok = min(tpt, C - tok0);        // >= 1: the tile holds a query of the chunk
-        // A negative scale enters as -Q (exact in bf16) against |scale|, so the row maximum is
-        // always taken over the scores as they are; such Q is negated on the way in, by threads.
-        const bool neg = a.scale_log2 < 0.f;
-        // a whole tile at a positive scale inside the rows the q map covers: Q by TMA (a chunk
-        // longer than max_chunk can put a later sequence's tiles past them)
-        const bool whole = ntok == tpt && !neg && q0 + tok0 + tpt <= a.q_rows;
         const bool valid = r < ntok * g;
         const int qi = r / g, h = r % g;
         const int pos = valid ? L - C + tok0 + qi : -1;  // causal limit of the row (inclusive)
@@ -374,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
         const uint32_t tm_row = tmem + lane_base;
         uint8_t* qs = smem + kOffQ;
         constexpr int bar_id = 1;                   // named barrier of the softmax warps
-        if (whole) {
+        if (whole && !neg) {
             if (r == 0) {
                 prefetch_tensormap(&tm_q);
                 mbar_arrive_expect_tx(&bars->q_full, kQTile);
@@ -494,14 +513,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
             if (all_ok) {
                 tc_fence_after();
                 const float inv = l > 0.f ? 1.f / l : 0.f;
-                // each thread stores its own row (256 contiguous bytes; the g rows of a query
-                // are one contiguous run)
-                __nv_bfloat16* dst = a.out + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD;
+                if (whole) {
+                    // The tile goes out by TMA through a map of out shaped like q's: each thread
+                    // writes its row, in bf16, into the Q buffer (free: every MMA has finished)
+                    // in the layout the load used, then one thread stores both column halves.
 #pragma unroll
-                for (int c = 0; c < kD; c += 32) {
-                    uint32_t o[32];
-                    tmem_ld32(tm_row + kTmemO + c, o);
-                    if (valid) {
+                    for (int c = 0; c < kD; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tm_row + kTmemO + c, o);
 #pragma unroll
                         for (int e = 0; e < 32; e += 8) {
                             uint4 v;
@@ -509,7 +528,35 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
                             v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
                             v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
                             v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                            *reinterpret_cast<uint4*>(dst + c + e) = v;
+                            const int cc = (c + e) >> 3;  // 16-byte chunk of the row, 0..15
+                            *reinterpret_cast<uint4*>(qs + (cc >> 3) * kQHalf + swz128(r, cc & 7)) = v;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    named_sync(bar_id, 128);
+                    if (r == 0) {
+                        tma_store_3d(&tm_o, 0, kvh * g, q0 + tok0, qs);
+                        tma_store_3d(&tm_o, 64, kvh * g, q0 + tok0, qs + kQHalf);
+                        bulk_commit();
+                        bulk_wait_read();  // the shared memory stays until the store has read it
+                    }
+                } else {
+                    // a tile cut short: each thread stores its own row (256 contiguous bytes)
+                    __nv_bfloat16* dst = a.out + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD;
+#pragma unroll
+                    for (int c = 0; c < kD; c += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(tm_row + kTmemO + c, o);
+                        if (valid) {
+#pragma unroll
+                            for (int e = 0; e < 32; e += 8) {
+                                uint4 v;
+                                v.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                                v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                                v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                                v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                                *reinterpret_cast<uint4*>(dst + c + e) = v;
+                            }
                         }
                     }
                 }
@@ -546,6 +593,8 @@ cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStre
     const long long tokens = (long long)a.batch * a.max_chunk;
     CUtensorMap tm_q;
     if (!rows_map(&tm_q, a.q, tokens, a.num_heads, kD, g, tpt)) return cudaErrorInvalidValue;
+    CUtensorMap tm_o;  // out, shaped like q: whole tiles are stored through it
+    if (!rows_map(&tm_o, a.out, tokens, a.num_heads, kD, g, tpt)) return cudaErrorInvalidValue;
     Tc2Args t;
     t.q = static_cast<const __nv_bfloat16*>(a.q);
     t.block_tables = a.block_tables;
@@ -573,7 +622,7 @@ cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStre
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_tc2_kernel, pool.tm_k, pool.tm_v, tm_q, t);
+    return cudaLaunchKernelEx(&cfg, prefill_tc2_kernel, pool.tm_k, pool.tm_v, tm_q, tm_o, t);
 }
 
 }  // namespace pa
