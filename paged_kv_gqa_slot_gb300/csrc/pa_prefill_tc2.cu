@@ -23,8 +23,10 @@
 // So S(j+1) is computed while the softmax works on stage j, and P V(j) only gates S(j+2),
 // which reuses the buffer P(j) sits in: the tensor core runs one issuer's MMAs in order, and
 // the MMA warp issues, per stage j, P V(j) then S(j+2).
-// The running max is re-based lazily: O is rescaled in TMEM only when a row's max grows by
-// more than 2^8, which keeps every P <= 256 and makes rescales rare.
+// The running max is re-based lazily: a stage is first taken against the row's current base,
+// and only a row's first visible stage, or a stage whose sum passes 2^16 in some row of the
+// warp, takes the row maximum; O is then rescaled in TMEM for rows whose maximum grew by more
+// than 2^8.  So every P <= 2^16, and both the maximum and the rescales are rare.
 // Q tiles come in by TMA through a 3-D map of q (d, head, token) whose box is one tile; a tile
 // cut short by the end of its chunk, one at a negative scale, or one past the rows the map
 // covers is copied in row by row by its softmax threads instead.  Each row of O is stored by
@@ -64,7 +66,8 @@ constexpr int kBarOff = kOffV + kVStages * kKVStage;
 // The dynamic shared memory starts 1024-byte aligned (the swizzled tiles need it; the kernel
 // checks), so no slack is added: two CTAs must fit an SM's 228 KB with 1 KB reserved each.
 constexpr int kSmemBytes = kBarOff + 256;
-constexpr float kRescaleThreshold = 8.f;        // log2 units
+constexpr float kRescaleThreshold = 8.f;        // log2 units: a re-base moves the base to the max
+constexpr float kSpecSumLimit = 65536.f;        // a stage sum past this takes the maximum path
 constexpr float kLog2e = 1.44269504088896340736f;
 
 struct Bars {
@@ -168,6 +171,23 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int x, i
                      reinterpret_cast<uint64_t>(map)),
                  "r"(x), "r"(y), "r"(z)
                  : "memory");
+}
+
+// P of a stage against base -nbase (stage_exps on the warp's path) and the sum of the rounded
+// values, so that the weights P V uses sum to l.
+__device__ __forceinline__ float stage_p(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int lim, float sl,
+                                         float nbase, bool unmasked, uint32_t (&pw)[kKeys / 2]) {
+    if (unmasked)
+        stage_exps<true>(s0, s1, lim, sl, nbase, pw);
+    else
+        stage_exps<false>(s0, s1, lim, sl, nbase, pw);
+    float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int w = 0; w < kKeys / 2; w += 2) {
+        add_bf16x2(ls[0], ls[1], pw[w]);
+        add_bf16x2(ls[2], ls[3], pw[w + 1]);
+    }
+    return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
 // O (the row's 128 fp32 columns of tensor memory at `taddr`) *= f, in 8-column pieces.
@@ -444,41 +464,42 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
             tmem_ld32_async(sbuf + 32, s1);
             tmem_wait_ld(s0);
             tmem_wait_ld(s1);
-            const float mx = unmasked ? stage_max<true>(s0, s1, lim) : stage_max<false>(s0, s1, lim);
-            const float mxs = mx == -INFINITY ? -INFINITY : mx * sl;  // log2 units
-            const float m_new = fmaxf(m_used, mxs);
-            const bool rebase = m_new > m_used + kRescaleThreshold;  // always for the first visible key
-            if (__any_sync(0xffffffffu, rebase && m_used != -INFINITY)) {
-                // O changes only once P V(j-1) -- which may still run, since S(j) was ready long
-                // before -- has finished: its commit is o_done phase j-1 (phases up to j-2 are
-                // complete, as S(j) was issued after P V(j-2), and P V(j) waits for this stage's
-                // P, so the parity cannot alias)
-                if (j > 0 && __any_sync(0xffffffffu, !mbar_wait(&bars->o_done, (j - 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                scale_o(tm_row + kTmemO, rebase && m_used != -INFINITY ? fast_exp2(m_used - m_new) : 1.f);
-            }
-            if (rebase) {
-                l *= m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
-                m_used = m_new;
-            }
-            const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+            // The stage goes against the row's current base first.  Its maximum -- and with it a
+            // possible re-base of O -- is taken only for a row's first visible stage, or when a
+            // row's sum passes 2^16 (a score more than 10 above the base): otherwise every
+            // p <= 2^16, far from overflow in P, l and O.  Both decisions are the warp's.
             uint32_t pw[kKeys / 2];
-            if (unmasked)
-                stage_exps<true>(s0, s1, lim, sl, nbase, pw);
-            else
-                stage_exps<false>(s0, s1, lim, sl, nbase, pw);
-            // The row sum adds the rounded values, so the weights P V uses sum to l; then P goes
-            // over the first 32 columns of the stage's buffer.
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int w = 0; w < kKeys / 2; w += 2) {
-                add_bf16x2(ls[0], ls[1], pw[w]);
-                add_bf16x2(ls[2], ls[3], pw[w + 1]);
+            float lsum = 0.f;
+            bool full = __any_sync(0xffffffffu, m_used == -INFINITY && lim >= 0);
+            if (!full) {
+                lsum = stage_p(s0, s1, lim, sl, m_used == -INFINITY ? 0.f : -m_used, unmasked, pw);
+                full = __any_sync(0xffffffffu, !(lsum <= kSpecSumLimit));
             }
-            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            if (full) {
+                const float mx = unmasked ? stage_max<true>(s0, s1, lim) : stage_max<false>(s0, s1, lim);
+                const float mxs = mx == -INFINITY ? -INFINITY : mx * sl;  // log2 units
+                const float m_new = fmaxf(m_used, mxs);
+                const bool rebase = m_new > m_used + kRescaleThreshold;  // always for the first visible key
+                if (__any_sync(0xffffffffu, rebase && m_used != -INFINITY)) {
+                    // O changes only once P V(j-1) -- which may still run, since S(j) was ready
+                    // long before -- has finished: its commit is o_done phase j-1 (phases up to
+                    // j-2 are complete, as S(j) was issued after P V(j-2), and P V(j) waits for
+                    // this stage's P, so the parity cannot alias)
+                    if (j > 0 && __any_sync(0xffffffffu, !mbar_wait(&bars->o_done, (j - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    scale_o(tm_row + kTmemO, rebase && m_used != -INFINITY ? fast_exp2(m_used - m_new) : 1.f);
+                }
+                if (rebase) {
+                    l *= m_used == -INFINITY ? 0.f : fast_exp2(m_used - m_new);
+                    m_used = m_new;
+                }
+                lsum = stage_p(s0, s1, lim, sl, m_used == -INFINITY ? 0.f : -m_used, unmasked, pw);
+            }
+            l += lsum;
+            // P goes over the first 32 columns of the stage's buffer
 #pragma unroll
             for (int i = 0; i < kKeys / 16; ++i)
                 tmem_st8_nowait(sbuf + 8 * i, pw[8 * i], pw[8 * i + 1], pw[8 * i + 2], pw[8 * i + 3], pw[8 * i + 4],
