@@ -98,10 +98,18 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """A source without its comments and blank lines: what a change to the kernel changes."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (line.split("//", 1)[0].rstrip() for line in text.splitlines())
+    return "\n".join(line for line in lines if line)
+
+
 def source_sha(kind: str) -> str:
+    """Hash of the kernel sources a profile's counters were taken on, comments aside."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[kind]:
-        h.update((ROOT / "paged_kv_gqa_slot_gb300" / "csrc" / f).read_bytes())
+        h.update(_code_only((ROOT / "paged_kv_gqa_slot_gb300" / "csrc" / f).read_text()).encode())
     return h.hexdigest()[:12]
 
 

@@ -29,8 +29,9 @@
 // than 2^8.  So every P <= 2^16, and both the maximum and the rescales are rare.
 // Q tiles come in by TMA through a 3-D map of q (d, head, token) whose box is one tile; a tile
 // cut short by the end of its chunk, one at a negative scale, or one past the rows the map
-// covers is copied in row by row by its softmax threads instead.  Each row of O is stored by
-// its thread.
+// covers is copied in row by row by its softmax threads instead.  O leaves the same way: a
+// whole tile is staged in bf16 in the then free Q buffer and stored by TMA through a map of
+// out shaped like q's; the rows of a tile cut short are stored by their threads.
 // Warp roles: 0-3 softmax (TMEM lanes 32w..32w+31), 4 MMA issue + TMEM owner, 5 TMA loads of
 // K, 6 TMA loads of V.  Every CTA loads its own K/V; the CTAs of one (sequence, kv head) --
 // and, with a shared prefix, of every sequence that shares it -- read the same pool blocks,
