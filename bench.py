@@ -99,9 +99,10 @@ def load_peaks():
 
 
 def _code_only(text: str) -> str:
-    """A source without its comments and blank lines: what a change to the kernel changes."""
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    lines = (line.split("//", 1)[0].rstrip() for line in text.splitlines())
+    """A source without its comments, blank lines and layout whitespace: what a change to the
+    kernel changes."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    lines = (" ".join(line.split("//", 1)[0].split()) for line in text.splitlines())
     return "\n".join(line for line in lines if line)
 
 

@@ -56,3 +56,17 @@ def test_reference_arm_runs_on_rank_0_only():
     import bench
     args = bench.argparse.Namespace(gpus=2, steps=1, warmup=3, impl="reference", no_cpu_baseline=True, only=None)
     assert bench.run_reference(args, 2, 1) == 0  # returns at once, no oracle work, no output
+
+
+def test_profile_traffic_is_keyed_to_code_not_comments():
+    """The DRAM traffic a committed ncu summary reports is used only while the kernel sources
+    hash the same, comments and blank lines aside: a comment edit keeps it, a code edit drops it."""
+    import bench
+    src = "int f(int x) {  // doubles\n\n    /* note */ return 2 * x;\n}\n"
+    same = "// a header line\nint f(int x) {  // twice x\n    return 2 * x;   \n}\n"
+    other = "int f(int x) {\n    return 3 * x;\n}\n"
+    assert bench._code_only(src) == bench._code_only(same)
+    assert bench._code_only(src) != bench._code_only(other)
+    # every committed summary's traffic line still matches its kernels' sources
+    for kind, workload in (("prefill", "chunked_prefill"), ("decode", "batched_decode"), ("splitkv", "splitkv_4x8192")):
+        assert bench.profiled_traffic(kind, workload) is not None, (kind, workload)
