@@ -30,10 +30,12 @@
 // Q tiles come in by TMA through a 3-D map of q (d, head, token) whose box is one tile; a tile
 // cut short by the end of its chunk, one at a negative scale, or one past the rows the map
 // covers is copied in row by row by its softmax threads instead.  O leaves the same way: a
-// whole tile is staged in bf16 in the then free Q buffer and stored by TMA through a map of
-// out shaped like q's; the rows of a tile cut short are stored by their threads.
+// whole tile is staged in bf16 in the then free Q buffer -- the softmax warps the first column
+// half of their rows, the four control warps (done with their roles) the second -- and stored
+// by TMA through a map of out shaped like q's; the rows of a tile cut short are stored by
+// their threads.
 // Warp roles: 0-3 softmax (TMEM lanes 32w..32w+31), 4 MMA issue + TMEM owner, 5 TMA loads of
-// K, 6 TMA loads of V.  Every CTA loads its own K/V; the CTAs of one (sequence, kv head) --
+// K, 6 TMA loads of V, 7 only the epilogue.  Every CTA loads its own K/V; the CTAs of one (sequence, kv head) --
 // and, with a shared prefix, of every sequence that shares it -- read the same pool blocks,
 // the copies after the first from L2.
 #include <algorithm>
@@ -52,7 +54,7 @@ constexpr int kKeys = 64;                       // keys per stage (MMA N of S, K
 constexpr int kKStages = 3, kVStages = 2;       // K and V ring slots (a third K slot measured 1% faster)
 constexpr int kSoftmaxThreads = 128;
 constexpr int kMmaWarp = kSoftmaxThreads / 32, kKLoadWarp = kMmaWarp + 1, kVLoadWarp = kMmaWarp + 2;
-constexpr int kThreads = kSoftmaxThreads + 96;
+constexpr int kThreads = kSoftmaxThreads + 128;  // warp 7 helps only with the epilogue
 constexpr int kCtasPerSm = 2;                   // resident CTAs an SM holds (tensor memory, shared memory)
 constexpr int kTmemCols = 256;                  // half of an SM's tensor memory
 constexpr uint32_t kTmemS = 0, kTmemO = 128;    // score buffers at 0 and 64, O at 128
@@ -66,7 +68,8 @@ constexpr int kOffV = kOffK + kKStages * kKVStage;
 constexpr int kBarOff = kOffV + kVStages * kKVStage;
 // The dynamic shared memory starts 1024-byte aligned (the swizzled tiles need it; the kernel
 // checks), so no slack is added: two CTAs must fit an SM's 228 KB with 1 KB reserved each.
-constexpr int kSmemBytes = kBarOff + 256;
+constexpr int kOffX = kBarOff + 256;           // [128] 1/l of every row, then the epilogue's path
+constexpr int kSmemBytes = kOffX + 528;
 constexpr float kRescaleThreshold = 8.f;        // log2 units: a re-base moves the base to the max
 constexpr float kSpecSumLimit = 65536.f;        // a stage sum past this takes the maximum path
 constexpr float kLog2e = 1.44269504088896340736f;
@@ -340,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
                     if (!mbar_wait(&full[j % nslots], (j / nslots) & 1)) ok = false;
                 if (!ok) atomicOr(a.status, kDevTimeout);
             }
-        } else {
+        } else if (warp == kMmaWarp) {
             // -------------------------------------------------------- MMA issue
             // The tile's chain -- P(j), then P V(j), then S(j+2) into the buffer P(j) held -- in
             // one warp; the other resident CTA's MMA warp keeps the tensor core busy while this
@@ -403,6 +406,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
             if (!mbar_wait_warp(&bars->drain, 0)) ok = false;
             if (!ok && lane == 0) atomicOr(a.status, kDevTimeout);
         }
+        // Epilogue: for a whole tile, the second column half of O of the lanes this warp may
+        // reach (quarter warp % 4), once the softmax warps have published 1/l of every row
+        float* xinv = reinterpret_cast<float*>(smem + kOffX);
+        const int* xflag = reinterpret_cast<const int*>(xinv + kRows);
+        named_sync(3, 256);
+        if (*xflag) {
+            tc_fence_after();
+            const int q = warp & 3, rr = 32 * q + lane;
+            const float inv = xinv[rr];
+            const uint32_t tm = tmem + ((uint32_t)(32 * q) << 16);
+            uint8_t* qs = smem + kOffQ;
+#pragma unroll
+            for (int c = 64; c < kD; c += 32) {
+                uint32_t o[32];
+                tmem_ld32(tm + kTmemO + c, o);
+#pragma unroll
+                for (int e = 0; e < 32; e += 8) {
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv);
+                    v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
+                    v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
+                    v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
+                    const int cc = (c + e) >> 3;
+                    *reinterpret_cast<uint4*>(qs + kQHalf + swz128(rr, cc & 7)) = v;
+                }
+            }
+            fence_proxy_async_smem();
+        }
+        named_sync(3, 256);
+        tc_fence_before();
     } else {
         // ------------------------------------------------------------ softmax: one row per thread
         const int r = threadIdx.x;                  // TMEM lane r, MMA row r
@@ -532,15 +565,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
             if (ok) ok = !__any_sync(0xffffffffu, !mbar_wait(&bars->o_final, 0));
             // one verdict for the softmax warps, which then take the same path
             const bool all_ok = named_sync_all(bar_id, 128, ok);
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float* xinv = reinterpret_cast<float*>(smem + kOffX);
+            int* xflag = reinterpret_cast<int*>(xinv + kRows);
+            // a whole tile: the control warps take the second column half of every quarter
+            xinv[r] = inv;
+            if (r == 0) *xflag = all_ok && whole;
+            named_sync(3, 256);
             if (all_ok) {
                 tc_fence_after();
-                const float inv = l > 0.f ? 1.f / l : 0.f;
                 if (whole) {
-                    // The tile goes out by TMA through a map of out shaped like q's: each thread
-                    // writes its row, in bf16, into the Q buffer (free: every MMA has finished)
-                    // in the layout the load used, then one thread stores both column halves.
 #pragma unroll
-                    for (int c = 0; c < kD; c += 32) {
+                    for (int c = 0; c < 64; c += 32) {
                         uint32_t o[32];
                         tmem_ld32(tm_row + kTmemO + c, o);
 #pragma unroll
@@ -550,18 +586,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
                             v.y = pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv);
                             v.z = pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv);
                             v.w = pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv);
-                            const int cc = (c + e) >> 3;  // 16-byte chunk of the row, 0..15
-                            *reinterpret_cast<uint4*>(qs + (cc >> 3) * kQHalf + swz128(r, cc & 7)) = v;
+                            const int cc = (c + e) >> 3;  // 16-byte chunk of the row, 0..7
+                            *reinterpret_cast<uint4*>(qs + swz128(r, cc)) = v;
                         }
                     }
                     fence_proxy_async_smem();
-                    named_sync(bar_id, 128);
-                    if (r == 0) {
-                        tma_store_3d(&tm_o, 0, kvh * g, q0 + tok0, qs);
-                        tma_store_3d(&tm_o, 64, kvh * g, q0 + tok0, qs + kQHalf);
-                        bulk_commit();
-                        bulk_wait_read();  // the shared memory stays until the store has read it
-                    }
                 } else {
                     // a tile cut short: each thread stores its own row (256 contiguous bytes)
                     __nv_bfloat16* dst = a.out + ((size_t)(q0 + tok0 + qi) * a.num_heads + (size_t)kvh * g + h) * kD;
@@ -582,6 +611,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
                         }
                     }
                 }
+            }
+            named_sync(3, 256);  // both column halves staged
+            if (all_ok && whole && r == 0) {
+                tma_store_3d(&tm_o, 0, kvh * g, q0 + tok0, qs);
+                tma_store_3d(&tm_o, 64, kvh * g, q0 + tok0, qs + kQHalf);
+                bulk_commit();
+                bulk_wait_read();  // the shared memory stays until the store has read it
             }
             if (!ok) atomicOr(a.status, kDevTimeout);
         }
