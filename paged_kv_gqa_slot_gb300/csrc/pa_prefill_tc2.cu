@@ -72,6 +72,7 @@ constexpr int kOffX = kBarOff + 256;           // [128] 1/l of every row, then t
 constexpr int kSmemBytes = kOffX + 528;
 constexpr float kRescaleThreshold = 8.f;        // log2 units: a re-base moves the base to the max
 constexpr float kSpecSumLimit = 65536.f;        // a stage sum past this takes the maximum path
+constexpr float kSplitScale = 2.f;              // |scale| sqrt(d) past this: P in two bf16 halves
 constexpr float kLog2e = 1.44269504088896340736f;
 
 struct Bars {
@@ -194,6 +195,35 @@ __device__ __forceinline__ float stage_p(const uint32_t (&s0)[32], const uint32_
     return (ls[0] + ls[1]) + (ls[2] + ls[3]);
 }
 
+// The low halves of P for a large scale: p again (the same operations as stage_exps, so the same
+// values), less its bf16 high half `pw`, rounded to bf16; written 8 words at a time to the
+// 32 columns at `dst` (the second half of the stage's buffer, free once S is in registers).
+// Returns the sum of the rounded low values.
+template <bool kAll>
+__device__ __forceinline__ float stage_lo(const uint32_t (&s0)[32], const uint32_t (&s1)[32], int lim, float sl,
+                                          float nbase, const uint32_t (&pw)[kKeys / 2], uint32_t dst) {
+    float ls[2] = {0.f, 0.f};
+#pragma unroll
+    for (int c0 = 0; c0 < kKeys; c0 += 16) {
+        uint32_t lw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int c = c0 + 2 * k;
+            float x0, x1;
+            fma_x2(x0, x1, score(s0, s1, c), score(s0, s1, c + 1), sl, sl, nbase, nbase);
+            if (!kAll) {
+                x0 = c > lim ? -INFINITY : x0;
+                x1 = c + 1 > lim ? -INFINITY : x1;
+            }
+            const uint32_t h = pw[c / 2];
+            lw[k] = pack_bf16x2(fast_exp2(x0) - bf16_lo(h), fast_exp2(x1) - bf16_hi(h));
+            add_bf16x2(ls[0], ls[1], lw[k]);
+        }
+        tmem_st8_nowait(dst + c0 / 2, lw[0], lw[1], lw[2], lw[3], lw[4], lw[5], lw[6], lw[7]);
+    }
+    return ls[0] + ls[1];
+}
+
 // O (the row's 128 fp32 columns of tensor memory at `taddr`) *= f, in 8-column pieces.
 __device__ __forceinline__ void scale_o(uint32_t taddr, float f) {
 #pragma unroll 1
@@ -208,6 +238,9 @@ __device__ __forceinline__ void scale_o(uint32_t taddr, float f) {
     tmem_wait_st();
 }
 
+// kSplit: P as bf16 high + low halves (two P V products), for a large scale.  A separate
+// instantiation, so the usual one carries none of that code.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                                            const __grid_constant__ CUtensorMap tm_v,
                                                                            const __grid_constant__ CUtensorMap tm_q,
@@ -376,6 +409,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
                 for (int kk = 0; kk < kKeys / 16; ++kk)
                     tc_mma_ts_ew(tmem + kTmemO, tm_p + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
                                  (j > 0 || kk > 0) ? 1u : 0u);
+                if (kSplit) {  // the low halves of P, against the same V
+#pragma unroll
+                    for (int kk = 0; kk < kKeys / 16; ++kk)
+                        tc_mma_ts_ew(tmem + kTmemO, tm_p + 32 + kk * 8, vd + (uint64_t)((kk * 16 * 128) >> 4), idesc_o,
+                                     1u);
+                }
                 tc_commit_ew(&bars->o_done);
                 tc_commit_ew(&bars->v_empty[j % kVStages]);
                 if (j + 1 == n) tc_commit_ew(&bars->o_final);
@@ -533,6 +572,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
                 lsum = stage_p(s0, s1, lim, sl, m_used == -INFINITY ? 0.f : -m_used, unmasked, pw);
             }
             l += lsum;
+            if (kSplit) {
+                // the low halves go over the second 32 columns; l sums them too, so the weights
+                // the two P V products apply still sum to l
+                const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+                l += unmasked ? stage_lo<true>(s0, s1, lim, sl, nbase, pw, sbuf + 32)
+                              : stage_lo<false>(s0, s1, lim, sl, nbase, pw, sbuf + 32);
+            }
             // P goes over the first 32 columns of the stage's buffer
 #pragma unroll
             for (int i = 0; i < kKeys / 16; ++i)
@@ -636,11 +682,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
 cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
     static OncePerDevice configured;
     const cudaError_t e = configured.run([] {
-        cudaError_t r = cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        // all of the SM's unified memory as shared memory, so that two CTAs fit
-        if (r == cudaSuccess)
-            r = cudaFuncSetAttribute(prefill_tc2_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     (int)cudaSharedmemCarveoutMaxShared);
+        cudaError_t r = cudaSuccess;
+        for (const void* fn : {(const void*)prefill_tc2_kernel<false>, (const void*)prefill_tc2_kernel<true>}) {
+            if (r == cudaSuccess) r = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            // all of the SM's unified memory as shared memory, so that two CTAs fit
+            if (r == cudaSuccess)
+                r = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+        }
         return r;
     });
     if (e != cudaSuccess) return e;
@@ -670,6 +719,10 @@ cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStre
     const int tiles = std::max(1, (a.max_chunk + tpt - 1) / tpt);
     t.batch = a.batch;
     t.tiles = tiles;
+    // Rounding P to bf16 perturbs each weight by up to 2^-9 of itself.  For a peaked softmax
+    // (scores spread much wider than 1/sqrt(d) would make them) that error on the few dominant
+    // weights approaches the output tolerance, so P is then also carried as a low half.
+    const bool split = std::fabs(a.scale) * std::sqrt((float)kD) > kSplitScale;
     const long long ctas = (long long)tiles * a.batch * pool.num_kv_heads;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;  // more CTAs than a grid holds
     cudaLaunchConfig_t cfg = {};
@@ -680,7 +733,8 @@ cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStre
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, prefill_tc2_kernel, pool.tm_k, pool.tm_v, tm_q, tm_o, t);
+    return split ? cudaLaunchKernelEx(&cfg, prefill_tc2_kernel<true>, pool.tm_k, pool.tm_v, tm_q, tm_o, t)
+                 : cudaLaunchKernelEx(&cfg, prefill_tc2_kernel<false>, pool.tm_k, pool.tm_v, tm_q, tm_o, t);
 }
 
 }  // namespace pa

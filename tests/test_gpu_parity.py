@@ -261,6 +261,19 @@ def test_prefill_late_dominant_keys_rebase():
     check_status_clean("late dominant keys")
 
 
+def test_prefill_large_scale_peaked_rows():
+    """Scores spread far wider than 1/sqrt(d) would make them (scale 0.25 at d = 128): a few
+    weights dominate each row, and the bf16 rounding of P alone took single elements at |o| ~ 2
+    past the 1e-2 bound (1.004e-2 and 1.079e-2, found by a random sweep of prefill shapes); the
+    prefill then carries P as bf16 high and low halves."""
+    for seed, kw in ((113006, dict(batch=4, num_heads=128, num_kv_heads=8, max_len=200, q_len=5)),
+                     (121020, dict(batch=6, num_heads=8, num_kv_heads=2, max_len=1300, q_len=400))):
+        case = W.random_case(seed, head_dim=128, min_len=1, prefill=True, scale=0.25, **kw)
+        g = GpuCase(case)
+        compare(g.prefill(), oracle_prefill(case), f"prefill scale 0.25, seed {seed}")
+    check_status_clean("large scale")
+
+
 def test_prefill_one_row_chunk_equals_decode():
     case = W.random_case(5100, batch=5, num_heads=32, num_kv_heads=8, head_dim=128, min_len=20, max_len=300)
     g = GpuCase(case)
