@@ -780,3 +780,38 @@ def test_alternate_prefill_kernels(impl, tmp_path):
     r = subprocess.run([sys.executable, str(script), root, impl], capture_output=True, text=True, timeout=600,
                        env=env)
     assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-4000:]
+
+
+def test_random_shape_sweep():
+    """Seeded random shapes across the paths: chunked prefills (group 1 to 32, shared prefixes,
+    short and long chunks, the usual, a negative and a large scale), split-KV partitions with
+    their merge (P from 1 to 32, d 64 and 128) and chunks of two to four queries --
+    each against the oracle.  The sweep that found the large-scale P rounding limit, kept small."""
+    import random
+    rng = random.Random(20261203)
+    for it in range(36):
+        hkv = rng.choice([1, 2, 4, 8])
+        g = rng.choice([1, 2, 4, 8, 16, 32])
+        if g * hkv > 128:
+            g = 128 // hkv
+        shared = rng.choice([0, 16, 48])
+        scale = rng.choice([None, None, -0.07, 0.25])
+        case = W.random_case(97000 + it, batch=rng.randint(1, 5), num_heads=g * hkv, num_kv_heads=hkv,
+                             head_dim=128, min_len=1 + shared, max_len=rng.choice([60, 300, 900]) + shared,
+                             q_len=rng.choice([5, 40, 200]), prefill=True, shared_prefix_tokens=shared, scale=scale)
+        compare(GpuCase(case).prefill(), oracle_prefill(case), f"random prefill {it}")
+        check_status_clean(f"random prefill {it}")
+    for it in range(24):
+        hkv = rng.choice([1, 2, 4, 8])
+        g = rng.choice([1, 2, 4, 8, 16])
+        d = rng.choice([64, 128])
+        scale = rng.choice([None, 0.25, -0.2])
+        case = W.random_case(98000 + it, batch=rng.randint(1, 6), num_heads=g * hkv, num_kv_heads=hkv, head_dim=d,
+                             min_len=1, max_len=rng.choice([40, 700, 3000]), scale=scale)
+        ws_o, ws_lse = GpuCase(case).splitkv(rng.choice([1, 2, 5, 8, 16, 32]))
+        compare(pa.pa_combine(ws_o, ws_lse), oracle_decode(case), f"random split-KV {it}")
+        pc = W.random_case(99000 + it, batch=rng.randint(1, 6), num_heads=g * hkv, num_kv_heads=hkv, head_dim=d,
+                           min_len=2, max_len=rng.choice([40, 700]), q_len=rng.choice([2, 3, 4]), prefill=True,
+                           scale=scale)
+        compare(GpuCase(pc).prefill(), oracle_prefill(pc), f"random short chunks {it}")
+        check_status_clean(f"random split-KV {it}")
