@@ -76,7 +76,7 @@ FULL_WORKLOADS = ("chunked_prefill",) + DECODE_WORKLOADS  # longest chain first
 KERNEL_SOURCES = {
     "decode": ["pa_decode.cu", "pa_block_attn.cuh", "pa_device.cuh"],
     "splitkv": ["pa_decode.cu", "pa_block_attn.cuh", "pa_device.cuh"],
-    "prefill": ["pa_prefill.cu", "pa_prefill_tc2.cu", "pa_block_attn.cuh", "pa_device.cuh"],
+    "prefill": ["pa_prefill_tc2.cu", "pa_device.cuh"],  # the tcgen05 kernel the profile covers
     "append": ["pa_append.cu", "pa_device.cuh"],
     "combine": ["pa_decode.cu", "pa_device.cuh"],
 }

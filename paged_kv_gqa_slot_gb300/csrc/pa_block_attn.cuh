@@ -15,7 +15,9 @@
 // computes S = Q K^T with mma.m16n8k16 (Q fragments stay in registers), masks, updates
 // the running max / sum (online softmax in base 2, fp32), rounds P to bf16 and
 // accumulates O += P V with the same MMA, reading K and V with ldmatrix (V transposed).
-// The running sum adds the bf16-rounded P, the very weights the P V product uses.
+// The running sum adds the bf16-rounded P, the very weights the P V product uses.  The
+// decode form (block_step_heads, below) carries P as high and low bf16 parts instead, two
+// P V products a block, so that O keeps about 16 bits of each weight.
 #pragma once
 
 #include "pa_device.cuh"
@@ -309,9 +311,14 @@ __device__ __forceinline__ void load_q_rows(uint32_t (&qb)[NT][D / 16][2], const
 }
 
 // One head column's update from this thread's two tokens (x0: token lane/4, x8: lane/4+8);
-// returns alpha and writes the two probabilities back into x0, x8, already rounded to bf16
-// (the P V operand), which is also what the running sum adds.
-__device__ __forceinline__ float head_update(float& m, float& l, float& x0, float& x8) {
+// returns alpha.  Each probability p is carried as two bf16 values, hi = bf16(p) in x0, x8
+// and lo = bf16(p - hi) in y0, y8 (p - hi is exact in fp32), which the P V product takes as
+// two MMAs: together they hold p to about 16 significant bits instead of 8, and the running
+// sum adds hi + lo, the weights the product uses.  With one bf16 P the weights of a row that
+// few keys dominate are off by up to 2^-9 of themselves, which moves O by up to 2^-9 times
+// the spread of those keys' V -- a few 1e-3 at unit-variance V, enough, added to the final
+// rounding of O to bf16, to cross a 1e-2 bound.
+__device__ __forceinline__ float head_update(float& m, float& l, float& x0, float& x8, float& y0, float& y8) {
     float mx = fmaxf(x0, x8);
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -319,9 +326,12 @@ __device__ __forceinline__ float head_update(float& m, float& l, float& x0, floa
     const float mn = fmaxf(m, mx);
     const float base = mn == -INFINITY ? 0.f : mn;
     const float alpha = fast_exp2(m - base);
-    x0 = round_bf16(fast_exp2(x0 - base));
-    x8 = round_bf16(fast_exp2(x8 - base));
-    l = l * alpha + (x0 + x8);
+    const float p0 = fast_exp2(x0 - base), p8 = fast_exp2(x8 - base);
+    x0 = round_bf16(p0);
+    x8 = round_bf16(p8);
+    y0 = round_bf16(p0 - x0);
+    y8 = round_bf16(p8 - x8);
+    l = l * alpha + ((x0 + y0) + (x8 + y8));
     m = mn;
     return alpha;
 }
@@ -332,7 +342,8 @@ __device__ __forceinline__ float head_update(float& m, float& l, float& x0, floa
 //                  V rows zeroed in the fragments, whatever the slot holds)
 // With MQ the columns are the (query, head) rows of a multi-query chunk: column j of this
 // thread in n-tile nt sees keys up to absolute position colpos[nt][j] (causal), and the
-// block's first key is at kbase.
+// block's first key is at kbase.  P is carried as high and low bf16 parts (head_update)
+// and the P V product runs once on each.
 template <int D, int NT, bool MQ = false>
 __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const uint32_t (&qb)[NT][D / 16][2],
                                                  float (&ot)[NT][D / 16][4], HeadState<NT>& hs, int valid,
@@ -355,7 +366,7 @@ __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const
     }
     const int t0 = lane >> 2;  // this thread's tokens: t0 and t0 + 8
     const bool v0 = t0 < valid, v8 = t0 + 8 < valid;
-    uint32_t pb[NT][2];
+    uint32_t pb[NT][2], pl[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         bool va0 = v0, va8 = v8, vb0 = v0, vb8 = v8;
@@ -368,8 +379,9 @@ __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const
         }
         float xa0 = va0 ? st[nt][0] * scale_log2 : -INFINITY, xa8 = va8 ? st[nt][2] * scale_log2 : -INFINITY;
         float xb0 = vb0 ? st[nt][1] * scale_log2 : -INFINITY, xb8 = vb8 ? st[nt][3] * scale_log2 : -INFINITY;
-        const float aa = head_update(hs.m[nt][0], hs.l[nt][0], xa0, xa8);
-        const float ab = head_update(hs.m[nt][1], hs.l[nt][1], xb0, xb8);
+        float ya0, ya8, yb0, yb8;
+        const float aa = head_update(hs.m[nt][0], hs.l[nt][0], xa0, xa8, ya0, ya8);
+        const float ab = head_update(hs.m[nt][1], hs.l[nt][1], xb0, xb8, yb0, yb8);
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
             ot[nt][mt][0] *= aa;
@@ -380,6 +392,8 @@ __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const
         // P^T rows (tokens) t0 / t0+8, columns (heads) 2t, 2t+1 -> transposed: the B operand
         pb[nt][0] = movmatrix_t(pack_bf16x2(xa0, xb0));
         pb[nt][1] = movmatrix_t(pack_bf16x2(xa8, xb8));
+        pl[nt][0] = movmatrix_t(pack_bf16x2(ya0, yb0));
+        pl[nt][1] = movmatrix_t(pack_bf16x2(ya8, yb8));
     }
     // V^T A fragments (ldmatrix.trans): matrices 0,1: tokens 0-7, 2,3: tokens 8-15;
     // 0,2: even d-chunk, 1,3: odd.  a0/a1 hold keys 2t, 2t+1; a2/a3 keys 2t+8, 2t+9.
@@ -400,7 +414,10 @@ __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const
         a2 &= m8;
         a3 &= m8;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(ot[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        for (int nt = 0; nt < NT; ++nt) {
+            mma_16816(ot[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            mma_16816(ot[nt][mt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
+        }
     }
 }
 

@@ -39,6 +39,7 @@
 // and, with a shared prefix, of every sequence that shares it -- read the same pool blocks,
 // the copies after the first from L2.
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstdlib>
 
@@ -73,6 +74,7 @@ constexpr int kSmemBytes = kOffX + 528;
 constexpr float kRescaleThreshold = 8.f;        // log2 units: a re-base moves the base to the max
 constexpr float kSpecSumLimit = 65536.f;        // a stage sum past this takes the maximum path
 constexpr float kSplitScale = 2.f;              // |scale| sqrt(d) past this: P in two bf16 halves
+constexpr int kFewKeys = 128;                   // a tile with a query that sees <= this: the same
 constexpr float kLog2e = 1.44269504088896340736f;
 
 struct Bars {
@@ -238,14 +240,15 @@ __device__ __forceinline__ void scale_o(uint32_t taddr, float f) {
     tmem_wait_st();
 }
 
-// kSplit: P as bf16 high + low halves (two P V products), for a large scale.  A separate
-// instantiation, so the usual one carries none of that code.
+__device__ __noinline__ void tc2_tile_split(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                            const CUtensorMap& tm_q, const CUtensorMap& tm_o, const Tc2Args& a);
+
+// One CTA's query tile.  kSplit: P as bf16 high + low halves (two P V products).  The
+// one-half form hands a tile with a query that sees at most kFewKeys keys (the first
+// queries of a sequence) to the two-halves form.
 template <bool kSplit>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                                           const __grid_constant__ CUtensorMap tm_v,
-                                                                           const __grid_constant__ CUtensorMap tm_q,
-                                                                           const __grid_constant__ CUtensorMap tm_o,
-                                                                           const __grid_constant__ Tc2Args a) {
+__device__ __forceinline__ void tc2_tile(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_q,
+                                         const CUtensorMap& tm_o, const Tc2Args& a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     Bars* bars = reinterpret_cast<Bars*>(smem + kBarOff);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -279,6 +282,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
     const int nblk = (nkeys + kBlockSize - 1) / kBlockSize;  // pool blocks read
     const int tok0 = mt * tpt;
     const int ntok = min(tpt, C - tok0);  // >= 1: the tile holds a query of the chunk
+    if (!kSplit && L - C + tok0 + 1 <= kFewKeys) {
+        tc2_tile_split(tm_k, tm_v, tm_q, tm_o, a);
+        return;
+    }
     // A negative scale enters as -Q (exact in bf16) against |scale|, so the row maximum is
     // always taken over the scores as they are; such Q is negated on the way in, by threads.
     const bool neg = a.scale_log2 < 0.f;
@@ -677,6 +684,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const
     }
 }
 
+// The two-halves tile as a function of its own: its code stays out of the way of the
+// one-half form's, whose instructions are fetched cold after an L2 flush (inlined side by
+// side, the two forms made a cold launch of the one-half form about 10 us slower, with a
+// fifth of the issue slots lost to instruction fetch).
+__device__ __noinline__ void tc2_tile_split(const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                            const CUtensorMap& tm_q, const CUtensorMap& tm_o, const Tc2Args& a) {
+    tc2_tile<true>(tm_k, tm_v, tm_q, tm_o, a);
+}
+
+// kSplitAll: every tile carries P as two halves (a large scale).  Otherwise only the tiles
+// with a query that sees at most kFewKeys keys do -- the first queries of a sequence.
+template <bool kSplitAll>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) prefill_tc2_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                                           const __grid_constant__ CUtensorMap tm_v,
+                                                                           const __grid_constant__ CUtensorMap tm_q,
+                                                                           const __grid_constant__ CUtensorMap tm_o,
+                                                                           const __grid_constant__ Tc2Args a) {
+    tc2_tile<kSplitAll>(tm_k, tm_v, tm_q, tm_o, a);
+}
+
 }  // namespace
 
 cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStream_t stream) {
@@ -719,9 +746,11 @@ cudaError_t launch_prefill_tc2(const PoolView& pool, const AttnArgs& a, cudaStre
     const int tiles = std::max(1, (a.max_chunk + tpt - 1) / tpt);
     t.batch = a.batch;
     t.tiles = tiles;
-    // Rounding P to bf16 perturbs each weight by up to 2^-9 of itself.  For a peaked softmax
-    // (scores spread much wider than 1/sqrt(d) would make them) that error on the few dominant
-    // weights approaches the output tolerance, so P is then also carried as a low half.
+    // Rounding P to bf16 perturbs each weight by up to 2^-9 of itself.  Where a few weights
+    // dominate a row -- a peaked softmax (scores spread much wider than 1/sqrt(d) would make
+    // them), or a query that sees only a few keys -- that error is not averaged away and
+    // approaches the output tolerance, so P is then also carried as a low half: in every tile
+    // at such a scale, else in the tiles that hold a sequence's first kFewKeys queries.
     const bool split = std::fabs(a.scale) * std::sqrt((float)kD) > kSplitScale;
     const long long ctas = (long long)tiles * a.batch * pool.num_kv_heads;
     if (ctas > 0x7fffffffLL) return cudaErrorInvalidValue;  // more CTAs than a grid holds

@@ -274,6 +274,35 @@ def test_prefill_large_scale_peaked_rows():
     check_status_clean("large scale")
 
 
+def test_decode_few_keys():
+    """Sequences of 2 to 4 tokens: a row's softmax then rests on a few weights, whose bf16
+    rounding (up to 2^-9 of each) is not averaged away.  With P as one bf16 value these seeds
+    put single elements past the 1e-2 bound, at the usual scale and at 0.25 (found with a numpy
+    model of that arithmetic; seed 97003 of the random sweep was 1.008e-2 off on the GPU).
+    Decode carries P as high and low bf16 parts."""
+    for seed, scale in ((7109, None), (7096, None), (7118, None), (7017, 0.25), (7068, 0.25)):
+        case = W.random_case(seed, batch=16, num_heads=32, num_kv_heads=8, head_dim=128, min_len=2, max_len=4,
+                             scale=scale)
+        compare(GpuCase(case).decode(), oracle_decode(case), f"decode few keys, seed {seed}")
+    check_status_clean("decode few keys")
+
+
+def test_prefill_first_queries_of_a_sequence():
+    """Whole prompts as one chunk: a sequence's first queries see 1, 2, 3 ... keys, the same
+    few-weight rows as a short decode, and with P as one bf16 value these seeds put single
+    elements past the bound (the numpy model again).  The tiles that hold a query seeing at
+    most 128 keys carry P as two halves; the last case mixes such tiles with long ones in one
+    launch."""
+    for seed, H, L in ((8036, 32, 40), (8120, 64, 24), (8102, 32, 24), (8111, 32, 24)):
+        case = W.paged_case(name="fresh", seed=seed, seq_lens=[L] * 8, q_lens=[L] * 8, new_lens=[L] * 8,
+                            num_heads=H, num_kv_heads=8, head_dim=128, num_blocks=64)
+        compare(GpuCase(case).prefill(), oracle_prefill(case), f"whole prompts, seed {seed}")
+    mixed = W.paged_case(name="mixed", seed=8200, seq_lens=[24, 900, 200, 1500, 130], q_lens=[24, 200, 200, 64, 9],
+                         new_lens=[24, 200, 200, 64, 9], num_heads=32, num_kv_heads=8, head_dim=128, num_blocks=256)
+    compare(GpuCase(mixed).prefill(), oracle_prefill(mixed), "fresh and cached prompts in one launch")
+    check_status_clean("first queries")
+
+
 def test_prefill_one_row_chunk_equals_decode():
     case = W.random_case(5100, batch=5, num_heads=32, num_kv_heads=8, head_dim=128, min_len=20, max_len=300)
     g = GpuCase(case)
