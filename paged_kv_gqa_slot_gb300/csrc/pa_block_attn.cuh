@@ -17,7 +17,8 @@
 // accumulates O += P V with the same MMA, reading K and V with ldmatrix (V transposed).
 // The running sum adds the bf16-rounded P, the very weights the P V product uses.  The
 // decode form (block_step_heads, below) carries P as high and low bf16 parts instead, two
-// P V products a block, so that O keeps about 16 bits of each weight.
+// P V products a block, so that O keeps about 16 bits of each weight (the multi-query form
+// keeps one part where every row sees many keys at the usual scale).
 #pragma once
 
 #include "pa_device.cuh"
@@ -310,8 +311,26 @@ __device__ __forceinline__ void load_q_rows(uint32_t (&qb)[NT][D / 16][2], const
     }
 }
 
-// One head column's update from this thread's two tokens (x0: token lane/4, x8: lane/4+8);
-// returns alpha.  Each probability p is carried as two bf16 values, hi = bf16(p) in x0, x8
+// One head column's update from this thread's two tokens (x0: token lane/4, x8: lane/4+8)
+// with P as one bf16 value: returns alpha and writes the two probabilities back into x0, x8,
+// rounded to bf16 (the P V operand), which is also what the running sum adds.
+__device__ __forceinline__ float head_update_one(float& m, float& l, float& x0, float& x8) {
+    float mx = fmaxf(x0, x8);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(m, mx);
+    const float base = mn == -INFINITY ? 0.f : mn;
+    const float alpha = fast_exp2(m - base);
+    x0 = round_bf16(fast_exp2(x0 - base));
+    x8 = round_bf16(fast_exp2(x8 - base));
+    l = l * alpha + (x0 + x8);
+    m = mn;
+    return alpha;
+}
+
+// The same update with P in two parts; returns alpha.  Each probability p is carried as two
+// bf16 values, hi = bf16(p) in x0, x8
 // and lo = bf16(p - hi) in y0, y8 (p - hi is exact in fp32), which the P V product takes as
 // two MMAs: together they hold p to about 16 significant bits instead of 8, and the running
 // sum adds hi + lo, the weights the product uses.  With one bf16 P the weights of a row that
@@ -342,9 +361,9 @@ __device__ __forceinline__ float head_update(float& m, float& l, float& x0, floa
 //                  V rows zeroed in the fragments, whatever the slot holds)
 // With MQ the columns are the (query, head) rows of a multi-query chunk: column j of this
 // thread in n-tile nt sees keys up to absolute position colpos[nt][j] (causal), and the
-// block's first key is at kbase.  P is carried as high and low bf16 parts (head_update)
-// and the P V product runs once on each.
-template <int D, int NT, bool MQ = false>
+// block's first key is at kbase.  With TWO, P is carried as high and low bf16 parts
+// (head_update) and the P V product runs once on each; without, as one (head_update_one).
+template <int D, int NT, bool MQ, bool TWO>
 __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const uint32_t (&qb)[NT][D / 16][2],
                                                  float (&ot)[NT][D / 16][4], HeadState<NT>& hs, int valid,
                                                  float scale_log2, const int (*colpos)[2] = nullptr,
@@ -379,9 +398,11 @@ __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const
         }
         float xa0 = va0 ? st[nt][0] * scale_log2 : -INFINITY, xa8 = va8 ? st[nt][2] * scale_log2 : -INFINITY;
         float xb0 = vb0 ? st[nt][1] * scale_log2 : -INFINITY, xb8 = vb8 ? st[nt][3] * scale_log2 : -INFINITY;
-        float ya0, ya8, yb0, yb8;
-        const float aa = head_update(hs.m[nt][0], hs.l[nt][0], xa0, xa8, ya0, ya8);
-        const float ab = head_update(hs.m[nt][1], hs.l[nt][1], xb0, xb8, yb0, yb8);
+        float ya0 = 0.f, ya8 = 0.f, yb0 = 0.f, yb8 = 0.f;
+        const float aa = TWO ? head_update(hs.m[nt][0], hs.l[nt][0], xa0, xa8, ya0, ya8)
+                             : head_update_one(hs.m[nt][0], hs.l[nt][0], xa0, xa8);
+        const float ab = TWO ? head_update(hs.m[nt][1], hs.l[nt][1], xb0, xb8, yb0, yb8)
+                             : head_update_one(hs.m[nt][1], hs.l[nt][1], xb0, xb8);
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
             ot[nt][mt][0] *= aa;
@@ -392,8 +413,10 @@ __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const
         // P^T rows (tokens) t0 / t0+8, columns (heads) 2t, 2t+1 -> transposed: the B operand
         pb[nt][0] = movmatrix_t(pack_bf16x2(xa0, xb0));
         pb[nt][1] = movmatrix_t(pack_bf16x2(xa8, xb8));
-        pl[nt][0] = movmatrix_t(pack_bf16x2(ya0, yb0));
-        pl[nt][1] = movmatrix_t(pack_bf16x2(ya8, yb8));
+        if (TWO) {
+            pl[nt][0] = movmatrix_t(pack_bf16x2(ya0, yb0));
+            pl[nt][1] = movmatrix_t(pack_bf16x2(ya8, yb8));
+        }
     }
     // V^T A fragments (ldmatrix.trans): matrices 0,1: tokens 0-7, 2,3: tokens 8-15;
     // 0,2: even d-chunk, 1,3: odd.  a0/a1 hold keys 2t, 2t+1; a2/a3 keys 2t+8, 2t+9.
@@ -416,7 +439,7 @@ __device__ __forceinline__ void block_step_heads(uint32_t ks, uint32_t vs, const
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             mma_16816(ot[nt][mt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
-            mma_16816(ot[nt][mt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
+            if (TWO) mma_16816(ot[nt][mt], a0, a1, a2, a3, pl[nt][0], pl[nt][1]);
         }
     }
 }

@@ -18,7 +18,9 @@
 //     workspace for pa_combine.
 #include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 
@@ -67,6 +69,7 @@ struct DecodeArgs {
     int max_blocks, num_heads, num_kv_heads, num_blocks, group;
     int stages;  // ring slots, a multiple of kConsumerWarps
     float scale_log2;
+    int p_two_parts;  // |scale| sqrt(d) is large: P in two bf16 parts in every CTA
     const uint4* k_new;  // fused append (decode only): [B, Hkv, D] bf16, or null
     const uint4* v_new;
     const int64_t* slots;  // [B]
@@ -74,6 +77,11 @@ struct DecodeArgs {
     void* k_pool;  // the pool, for the fused append's row write
     void* v_pool;
 };
+
+// Where a multi-query chunk may keep P as one bf16 part: every row sees more than kFewKeys
+// keys and |scale| sqrt(d) <= kTwoPartScale (the same bounds as the tensor-core prefill's).
+constexpr int kFewKeys = 128;
+constexpr float kTwoPartScale = 2.f;
 
 template <int D, int NT, bool SPLIT, bool MQ>
 __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -210,18 +218,28 @@ __global__ void __launch_bounds__(kThreads, 4) decode_kernel(const __grid_consta
             load_q_heads<D, NT>(qb, a.q + ((size_t)b * a.num_heads + (size_t)kvh * g) * D, g);
         }
         bool ok = true;
-        for (int i = warp; i < n; i += kConsumerWarps) {
-            const int st = i % stages;
-            ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / stages) & 1));
-            if (!ok) break;
-            uint8_t* kt = smem + st * KvTile<D>::kStageBytes;
-            uint8_t* vt = kt + KvTile<D>::kTileBytes;
-            const int valid = min(kBlockSize, L - (blk0 + i) * kBlockSize);
-            block_step_heads<D, NT, MQ>(smem_u32(kt), smem_u32(vt), qb, ot, hs, valid, a.scale_log2, colpos,
-                                        (blk0 + i) * kBlockSize);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[st]);
-        }
+        auto consume = [&](auto two) {
+            for (int i = warp; i < n; i += kConsumerWarps) {
+                const int st = i % stages;
+                ok = __all_sync(0xffffffffu, mbar_wait(&full[st], (i / stages) & 1));
+                if (!ok) break;
+                uint8_t* kt = smem + st * KvTile<D>::kStageBytes;
+                uint8_t* vt = kt + KvTile<D>::kTileBytes;
+                const int valid = min(kBlockSize, L - (blk0 + i) * kBlockSize);
+                block_step_heads<D, NT, MQ, decltype(two)::value>(smem_u32(kt), smem_u32(vt), qb, ot, hs, valid,
+                                                                  a.scale_log2, colpos, (blk0 + i) * kBlockSize);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st]);
+            }
+        };
+        // P in two bf16 parts, except in a multi-query chunk whose every row sees more than
+        // kFewKeys keys at the usual scale: there the one-part rounding averages away, and the
+        // chunk's extra columns make the second P V product cost (the same CTA-uniform choice
+        // in every CTA of the sequence).
+        if (MQ && !a.p_two_parts && L - C + 1 > kFewKeys)
+            consume(std::false_type{});
+        else
+            consume(std::true_type{});
         if (!ok && lane == 0) atomicOr(a.status, kDevTimeout);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -495,6 +513,7 @@ cudaError_t launch_one(const PoolView& pool, const AttnArgs& a, int grid_x, int 
     da.num_blocks = pool.num_blocks;
     da.group = a.num_heads / pool.num_kv_heads;
     da.scale_log2 = a.scale * kLog2e;
+    da.p_two_parts = std::fabs(a.scale) * std::sqrt((float)D) > kTwoPartScale ? 1 : 0;
     da.stages = stages_for<D>(grid_x * pool.num_kv_heads * a.batch);
     da.k_new = static_cast<const uint4*>(a.k_new);
     da.v_new = static_cast<const uint4*>(a.v_new);
