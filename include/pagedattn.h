@@ -13,7 +13,12 @@
  *     o = sum_{t in keys} softmax_t(scale * <q, K_t>) V_t
  *
  * K_t, V_t read at pool[block_tables[s][t / 16], h / g, t % 16, :].  Softmax in fp32
- * (online, base 2), bf16 inputs, bf16 output rounded to nearest even.
+ * (online, base 2), bf16 inputs, bf16 output rounded to nearest even.  The probabilities
+ * enter the P V product on the tensor cores as bf16 -- as two bf16 parts (about 16 bits)
+ * wherever a few weights can dominate a row: always in pa_decode, pa_decode_splitkv and
+ * pa_append_decode, and in pa_prefill_chunked for the query tiles holding a query that sees
+ * at most 128 keys, or everywhere at |scale| sqrt(head_dim) > 2 -- with the softmax sum
+ * taken over exactly those values; accumulation is fp32.
  *
  * Memory.  Every pointer argument is a DEVICE pointer of the current CUDA device
  * unless stated otherwise; the caller allocates and owns every buffer (the library
