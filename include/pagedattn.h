@@ -16,9 +16,10 @@
  * (online, base 2), bf16 inputs, bf16 output rounded to nearest even.  The probabilities
  * enter the P V product on the tensor cores as bf16 -- as two bf16 parts (about 16 bits)
  * wherever a few weights can dominate a row: always in pa_decode, pa_decode_splitkv and
- * pa_append_decode, and in pa_prefill_chunked for the query tiles holding a query that sees
- * at most 128 keys, or everywhere at |scale| sqrt(head_dim) > 2 -- with the softmax sum
- * taken over exactly those values; accumulation is fp32.
+ * pa_append_decode; in pa_prefill_chunked always at head_dim 64 or a group size that does
+ * not divide 128, else in the query tiles holding a query that sees at most 128 keys, and
+ * everywhere at |scale| sqrt(head_dim) > 2 -- with the softmax sum taken over exactly those
+ * values; accumulation is fp32.
  *
  * Memory.  Every pointer argument is a DEVICE pointer of the current CUDA device
  * unless stated otherwise; the caller allocates and owns every buffer (the library

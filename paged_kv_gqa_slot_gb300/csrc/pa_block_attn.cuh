@@ -13,12 +13,12 @@
 //
 // Consumer: a warp owns a 16-row tile of (query, head) rows.  Per 16-token block it
 // computes S = Q K^T with mma.m16n8k16 (Q fragments stay in registers), masks, updates
-// the running max / sum (online softmax in base 2, fp32), rounds P to bf16 and
-// accumulates O += P V with the same MMA, reading K and V with ldmatrix (V transposed).
-// The running sum adds the bf16-rounded P, the very weights the P V product uses.  The
-// decode form (block_step_heads, below) carries P as high and low bf16 parts instead, two
-// P V products a block, so that O keeps about 16 bits of each weight (the multi-query form
-// keeps one part where every row sees many keys at the usual scale).
+// the running max / sum (online softmax in base 2, fp32), splits P into high and low bf16
+// parts and accumulates O += P V with the same MMA, once on each part, reading K and V with
+// ldmatrix (V transposed): O keeps about 16 bits of each weight.  The running sum adds
+// hi + lo, the very weights the products use.  The decode form (block_step_heads, below)
+// does the same (its multi-query use keeps one part where every row sees many keys at the
+// usual scale).
 #pragma once
 
 #include "pa_device.cuh"
@@ -123,9 +123,11 @@ __device__ __forceinline__ void mma_rows(float (&c)[Rows<TWO_ROWS>::kC], const u
 }
 
 // Online-softmax update of one row from its four scores in this thread (keys t0, t0+1,
-// t0+8, t0+9 of the block); returns the two packed bf16 P pairs and rescales o_row.
+// t0+8, t0+9 of the block); returns P's two packed bf16 pairs, as high parts (p01, p89) and
+// low parts (q01, q89: bf16(p - hi)), and alpha.  The running sum adds hi + lo, the weights
+// the two P V products apply.
 struct RowUpdate {
-    uint32_t p01, p89;
+    uint32_t p01, p89, q01, q89;
     float alpha;
 };
 __device__ __forceinline__ RowUpdate row_update(float& m, float& l, float s0, float s1, float s8, float s9, int t0,
@@ -141,14 +143,20 @@ __device__ __forceinline__ RowUpdate row_update(float& m, float& l, float s0, fl
     const float base = mn == -INFINITY ? 0.f : mn;  // a row that has seen no key yet
     RowUpdate u;
     u.alpha = fast_exp2(m - base);
-    x0 = round_bf16(fast_exp2(x0 - base));
-    x1 = round_bf16(fast_exp2(x1 - base));
-    x2 = round_bf16(fast_exp2(x2 - base));
-    x3 = round_bf16(fast_exp2(x3 - base));
-    l = l * u.alpha + ((x0 + x1) + (x2 + x3));
+    const float p0 = fast_exp2(x0 - base), p1 = fast_exp2(x1 - base);
+    const float p2 = fast_exp2(x2 - base), p3 = fast_exp2(x3 - base);
+    x0 = round_bf16(p0);
+    x1 = round_bf16(p1);
+    x2 = round_bf16(p2);
+    x3 = round_bf16(p3);
+    const float y0 = round_bf16(p0 - x0), y1 = round_bf16(p1 - x1);
+    const float y2 = round_bf16(p2 - x2), y3 = round_bf16(p3 - x3);
+    l = l * u.alpha + (((x0 + y0) + (x1 + y1)) + ((x2 + y2) + (x3 + y3)));
     m = mn;
     u.p01 = pack_bf16x2(x0, x1);
     u.p89 = pack_bf16x2(x2, x3);
+    u.q01 = pack_bf16x2(y0, y1);
+    u.q89 = pack_bf16x2(y2, y3);
     return u;
 }
 
@@ -187,7 +195,7 @@ __device__ __forceinline__ void block_step(uint32_t ks, uint32_t vs,
         }
     }
     const int t0 = (lane & 3) * 2;  // this thread's key columns: t0, t0+1, t0+8, t0+9
-    uint32_t pa[Rows<TWO_ROWS>::kA];
+    uint32_t pa[Rows<TWO_ROWS>::kA], pl[Rows<TWO_ROWS>::kA];  // P's high and low parts
     {
         const RowUpdate u = row_update(rs.m_a, rs.l_a, s0[0], s0[1], s1[0], s1[1], t0, lim_a, scale_log2);
 #pragma unroll
@@ -198,9 +206,13 @@ __device__ __forceinline__ void block_step(uint32_t ks, uint32_t vs,
         if constexpr (TWO_ROWS) {
             pa[0] = u.p01;
             pa[2] = u.p89;
+            pl[0] = u.q01;
+            pl[2] = u.q89;
         } else {
             pa[0] = u.p01;
             pa[1] = u.p89;
+            pl[0] = u.q01;
+            pl[1] = u.q89;
         }
     }
     if constexpr (TWO_ROWS) {
@@ -212,6 +224,8 @@ __device__ __forceinline__ void block_step(uint32_t ks, uint32_t vs,
         }
         pa[1] = u.p01;
         pa[3] = u.p89;
+        pl[1] = u.q01;
+        pl[3] = u.q89;
     }
     {
         const int mi = lane >> 3, rr = lane & 7;
@@ -231,6 +245,8 @@ __device__ __forceinline__ void block_step(uint32_t ks, uint32_t vs,
             ldsm_x4_t(addr, b0, b1, b2, b3);
             mma_rows<TWO_ROWS>(o[2 * nn], pa, b0 & m0, b1 & m1);
             mma_rows<TWO_ROWS>(o[2 * nn + 1], pa, b2 & m0, b3 & m1);
+            mma_rows<TWO_ROWS>(o[2 * nn], pl, b0 & m0, b1 & m1);
+            mma_rows<TWO_ROWS>(o[2 * nn + 1], pl, b2 & m0, b3 & m1);
         }
     }
 }

@@ -292,10 +292,13 @@ def test_prefill_first_queries_of_a_sequence():
     few-weight rows as a short decode, and with P as one bf16 value these seeds put single
     elements past the bound (the numpy model again).  The tiles that hold a query seeing at
     most 128 keys carry P as two halves; the last case mixes such tiles with long ones in one
-    launch."""
-    for seed, H, L in ((8036, 32, 40), (8120, 64, 24), (8102, 32, 24), (8111, 32, 24)):
+    launch.  Head dim 64 and groups that do not divide 128 (3, 6) run on the warp-MMA kernel,
+    which carries two parts throughout."""
+    for seed, H, hkv, d, L in ((8036, 32, 8, 128, 40), (8120, 64, 8, 128, 24), (8102, 32, 8, 128, 24),
+                               (8111, 32, 8, 128, 24), (8339, 16, 4, 64, 24), (8301, 24, 8, 128, 24),
+                               (8300, 48, 8, 64, 24)):
         case = W.paged_case(name="fresh", seed=seed, seq_lens=[L] * 8, q_lens=[L] * 8, new_lens=[L] * 8,
-                            num_heads=H, num_kv_heads=8, head_dim=128, num_blocks=64)
+                            num_heads=H, num_kv_heads=hkv, head_dim=d, num_blocks=64)
         compare(GpuCase(case).prefill(), oracle_prefill(case), f"whole prompts, seed {seed}")
     mixed = W.paged_case(name="mixed", seed=8200, seq_lens=[24, 900, 200, 1500, 130], q_lens=[24, 200, 200, 64, 9],
                          new_lens=[24, 200, 200, 64, 9], num_heads=32, num_kv_heads=8, head_dim=128, num_blocks=256)
