@@ -246,9 +246,10 @@ int pa_decode_num_splits(int32_t batch, int32_t num_kv_heads, int32_t max_blocks
 
 /*
  * Partition count suggested for pa_decode_splitkv on the current device (1..16): the
- * largest power of two, at most 16, whose CTAs (batch x num_kv_heads x count) fit one wave
- * of four per SM, keeping >= 8 blocks per partition (the library runs each partition on a
- * thread-block cluster of up to 4 CTAs when the partitions alone leave the wave short).
+ * largest count, at most 16, whose CTAs (batch x num_kv_heads x count) fill no more than
+ * four fifths of one wave of four per SM, keeping >= 8 blocks per partition (the library
+ * runs each partition on a thread-block cluster of up to 4 CTAs when the partitions alone
+ * leave the wave at least half empty).
  */
 int pa_splitkv_num_partitions(int32_t batch, int32_t num_kv_heads, int32_t max_blocks);
 

@@ -600,18 +600,19 @@ int decode_splits_for(int batch, int num_kv_heads, int max_blocks) {
 }
 
 int splitkv_partitions_for(int batch, int num_kv_heads, int max_blocks) {
-    // CTAs per (sequence, kv head) pair: the largest power of two whose CTAs fit one wave of
-    // four per SM; the partitions are that many up to 16, and a thread-block cluster per
-    // partition takes the rest (splitkv_cluster_for).  Measured on GB300 (152 SMs, 134 MB of
-    // KV): 4 x 8192 over 8 kv heads runs 27.2 us at P = 16 (512 CTAs) against 28.7 us at
-    // P = 19 (608); 1 x 32768 runs 27.0 us at P = 16 with 4-CTA clusters against 28.7 us at
-    // P = 32 with 2-CTA clusters and 40.6 us at P = 19 with 4-CTA clusters (608 CTAs, which
-    // do not all fit as clusters at once).  At least 8 blocks per partition.
+    // Partitions per (sequence, kv head) pair: as many as fill four fifths of one wave of four
+    // CTAs per SM, up to 16; a thread-block cluster per partition takes the rest of the wave
+    // when the partitions alone leave it at least half empty (splitkv_cluster_for).  Measured
+    // on GB300 (152 SMs, 134 MB of KV, per call with the merge, means of 60 in-graph samples):
+    // 4 x 8192 over 8 kv heads runs 28.4-28.7 us at P = 15 (480 CTAs), 28.9-29.2 at 14 and
+    // 29.3-30.4 at 16 (512), about 30.5 at 10; P = 19 (608, the whole wave) ran 28.7 against
+    // 27.2 at 16 in an earlier sweep, 24 and 32 slower still.  1 x 32768 runs its 16
+    // partitions on 4-CTA clusters (512 CTAs); 13-15 partitions there measured within half a
+    // microsecond of it, and 19 partitions on 4-CTA clusters (608 CTAs, which do not all fit
+    // as clusters at once) 40.6 us.  At least 8 blocks per partition.
     const int items = std::max(1, batch * num_kv_heads);
-    const int fit = std::max(1, (4 * device_info().num_sms) / items);
-    int p = 1;
-    while (p * 2 <= fit && p * 2 <= 16) p *= 2;
-    while (p > 1 && max_blocks / p < 8) p /= 2;
+    int p = std::max(1, std::min(16, (16 * device_info().num_sms) / (5 * items)));
+    while (p > 1 && max_blocks / p < 8) --p;
     return p;
 }
 
